@@ -1,0 +1,235 @@
+/*
+ * hs_api.h -- C ABI of libhs: the HiSparse top-k sparse decode hot path on
+ * GB300 (sm_103a).  One decode step is four stages:
+ *
+ *   S1 hs_normalize_indices   candidate union/dedup/validation, token -> slot
+ *   S2 hs_hot_lookup_assign   hot-buffer lookup keyed by global slot id, LRU
+ *   S3 hs_swap_in / hs_backup pinned host pool <-> HBM hot region row copies
+ *   S4 hs_sparse_decode       softmax(q K_S^T scale) V_S, split-KV merged
+ *
+ * Sources (web pages, cited by title and section):
+ *   [HS] vLLM HiSparse walkthrough (devpress.csdn.net): "Hisparse hot cache
+ *        初始化", "swap_in 方法流程详解", "triton_convert_req_index_to_global_index",
+ *        hisparse_swap_in_kernel Phase 1 .. Phase 5.
+ *   [HC] SGLang PR "[HiCache] TMA-staged host<->device KV transfer kernel
+ *        (sm_90+) - #40278": Motivation, Modifications.
+ *   [PT] PaperTrace 5.1.1 "从索引到 Kernel": sections 1.1-1.2 (eqs. 1-2),
+ *        3.1-3.2 (eqs. 4-7), 7.3 (eqs. 16-17, empty and illegal sets).
+ *   [PA] "PagedAttention 与 RadixAttention：上游机制与海光实现对照": 1.3, 1.4.
+ *
+ * Conventions, for every entry point:
+ *  - All buffers are caller-owned.  Device pointers are CUDA device memory;
+ *    "host pool" pointers are the DEVICE-VISIBLE address of pinned host
+ *    memory (see hs_host_device_pointer).  The library allocates nothing.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  The return value reports only the synchronous
+ *    host-side argument checks and the launch itself.
+ *  - Conditions found on the device (invalid indices, timeouts) are written
+ *    to caller-provided counters or a status word, readable after the stream
+ *    is synchronised.  Invalid indices are dropped and counted, never read
+ *    ([PT] 7.3: never silently read page 0; a wrong-request page is an error).
+ *  - Layouts are row-major and densely packed unless a stride is passed.
+ */
+#ifndef HS_API_H
+#define HS_API_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* hs_stream_t; /* identical to cudaStream_t */
+
+/* Status codes (return values, and the device status word). */
+#define HS_OK 0
+#define HS_ERR_INVALID_ARG 1  /* null pointer, negative size, overflow        */
+#define HS_ERR_MISALIGNED 2   /* row_bytes % 16 != 0 or unaligned pointer     */
+#define HS_ERR_CAPACITY 3     /* cap / hot_size / shared-memory limits        */
+#define HS_ERR_CUDA 4         /* a CUDA runtime call or launch failed         */
+#define HS_ERR_TIMEOUT 5      /* device: a bounded wait gave up               */
+#define HS_ERR_BAD_INDEX 6    /* device: an index outside its buffer, skipped */
+#define HS_ERR_UNSUPPORTED 7  /* a shape no kernel here implements            */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* hs_status_string(int status);
+
+/* Device-visible address of pinned host memory (cudaHostGetDevicePointer).
+ * host_ptr must come from cudaHostAlloc / cudaHostRegister (torch
+ * pin_memory()).  Returns HS_ERR_CUDA if the memory is not mapped. */
+int hs_host_device_pointer(const void* host_ptr, void** dev_ptr);
+
+/* ---------------------------------------------------------------------------
+ * S1  hs_normalize_indices -- [PT] 1.1 eq. (1) S = unique(D u W u A), 1.2
+ * eq. (2) b = floor(t / B), 7.3 eq. (16)/(17); [HS]
+ * triton_convert_req_index_to_global_index (slot = table[b] * B + t mod B).
+ *
+ * cand        int32 [rows, n_cand] dynamic candidates (token positions);
+ *             -1 is padding and is skipped silently.
+ * window      W: positions [max(0, T - W), T) join every row (0 = none).
+ * num_sinks   A: positions [0, min(A, T)) join every row (0 = none).
+ * row_req     int32 [rows]: request of each index row (several index rows
+ *             may share a request, e.g. one row per KV head).
+ * seq_lens    int32 [num_reqs]: T, the request's context length including
+ *             the newest token; a position is causal iff 0 <= t < T.
+ * block_table int32 [num_reqs, bt_stride]: logical block -> physical page;
+ *             only the first max_blocks entries of a row are read.
+ * page_owner  int32 [num_pages] or NULL: request that owns each page; when
+ *             given, a page owned by another request is rejected.
+ * cap         row capacity of the outputs; must be >= n_cand + window +
+ *             num_sinks (else HS_ERR_CAPACITY), so no valid set can overflow.
+ * out_tok     int32 [rows, cap]: S in ascending token order, -1 padded.
+ * out_slot    int32 [rows, cap]: global slot table[t / B] * B + t mod B, -1 padded.
+ * out_count   int32 [rows]: |S|.
+ * err_counts  int32 [rows, 4]: rejected positions per row, by first failing
+ *             check: [0] range (t < -1 or t < 0 from W/A, block >= max_blocks,
+ *             page outside [0, num_pages), row_req outside [0, num_reqs)),
+ *             [1] causal (t >= T), [2] owner, [3] duplicates (valid dynamic
+ *             entries already in S from W, A or an earlier dynamic entry).
+ * Output is bit-exact and independent of thread scheduling.
+ * ------------------------------------------------------------------------- */
+int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n_cand, int32_t window,
+                         int32_t num_sinks, const int32_t* row_req, const int32_t* seq_lens,
+                         const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                         const int32_t* page_owner, int32_t num_reqs, int32_t num_pages,
+                         int32_t page_size, int32_t cap, int32_t* out_tok, int32_t* out_slot,
+                         int32_t* out_count, int32_t* err_counts, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Hot-buffer state reset ([HS] "Hisparse hot cache初始化": the hot cache is
+ * zero-initialised; the coordinator invalidates recycled slots before reuse).
+ * dgi int32 [rows, hot_size] := -1 (empty); lru int16 [rows, hot_size] :=
+ * 0, 1, .., hot_size-1 (identity order).  hot_size <= 32767.
+ * ------------------------------------------------------------------------- */
+int hs_hot_state_reset(int32_t* dgi, int16_t* lru, int32_t rows, int32_t hot_size,
+                       hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * S2  hs_hot_lookup_assign -- [HS] hisparse_swap_in_kernel Phase 1 .. 4.
+ *
+ * Row r (one request) owns hot rows [r*region_stride, r*region_stride +
+ * hot_size]; the last one (hot_base + hot_size) is reserved for the newest
+ * token.  region_stride >= hot_size + 1 (the page uses hot_size + 1 rounded
+ * up to 128; any larger stride is accepted).
+ *
+ * slot        int32 [rows, cap]: global slot ids (S1 out_slot), -1 = none.
+ * count       int32 [rows] or NULL: entries i >= count[r] are treated as -1.
+ * num_real_rows rows r >= num_real_rows (CUDA-graph padding) output -1 and
+ *             keep their state.
+ * newest_slot int32 [rows] or NULL: the newest token's slot (the engine's
+ *             slot_mapping); it resolves to the reserved row and never
+ *             enters dgi / lru.
+ * dgi, lru    state, updated in place; lru must be a permutation of
+ *             0..hot_size-1 and the valid (>= 0) dgi values of a row unique,
+ *             which hs_hot_state_reset and this function maintain.
+ * hot_idx     int32 [rows, cap]: hot row of each entry, or -1.
+ * miss_mask   uint8 [rows, cap] or NULL: 1 where the entry was a miss.
+ * miss_src    int32 [rows, cap]: global slot of miss m, in row order.
+ * miss_dst    int64 [rows, cap]: hot row of miss m.
+ * miss_count  int32 [rows]: M, the number of misses of row r.
+ * stats       int64 [2]: {hits, misses} accumulated (atomically added).
+ * err         int32 [rows]: entries dropped as repeats of an earlier entry
+ *             of the row (only the first occurrence resolves).
+ * Semantics (bit-exact): walk lru from least to most recently used; a slot
+ * whose dgi is among the row's pending ids is a hit; the rest, in LRU order,
+ * are the evictable list E.  Misses, in row order m = 0, 1, .., take E[m].
+ * New lru = E[M:] ++ E[:M] ++ hits.  Requires cap <= hot_size (capacity).
+ * ------------------------------------------------------------------------- */
+int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows, int32_t cap,
+                         int32_t num_real_rows, const int32_t* newest_slot, int32_t* dgi,
+                         int16_t* lru, int32_t hot_size, int64_t region_stride,
+                         int32_t* hot_idx, uint8_t* miss_mask, int32_t* miss_src,
+                         int64_t* miss_dst, int32_t* miss_count, int64_t* stats, int32_t* err,
+                         hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * S3  hs_swap_in -- [HS] Phase 5 (copy each miss row host -> hot; a source
+ * outside [0, host_rows) zeroes the hot row and revokes its slot, dgi = -1),
+ * [HC] Modifications (TMA bulk copies staged through a shared-memory ring,
+ * one bulk op per contiguous run, per-row ops for scattered rows).
+ *
+ * host_pool   device-visible pointer to the pinned host pool, host_rows rows
+ *             of row_bytes each (16-byte aligned base).
+ * hot         device hot buffer, rows of row_bytes.
+ * row_bytes   multiple of 16 ([HS] HiSparseCoordinator rejects others).
+ * miss_src/miss_dst/miss_count  as produced by hs_hot_lookup_assign.
+ * dgi         int32 [rows, hot_size] or NULL: revocation target.
+ * status      int32 device word or NULL: HS_ERR_TIMEOUT / HS_ERR_BAD_INDEX
+ *             is stored there (first error wins) if the device hits one.
+ * Destinations must be distinct within one call.
+ * ------------------------------------------------------------------------- */
+int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, int64_t row_bytes,
+               const int32_t* miss_src, const int64_t* miss_dst, const int32_t* miss_count,
+               int32_t rows, int32_t cap, int32_t* dgi, int32_t hot_size, int64_t region_stride,
+               int32_t* status, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hs_backup -- [HS] overview "BackUp": after each step copy the newly
+ * generated KV row to host memory.  host_pool[dst_slots[i]] := src[src_rows[i]]
+ * for i < n.  src is a device buffer of rows of row_bytes; src_rows int64 [n]
+ * and dst_slots int32 [n] are device arrays.  A destination outside
+ * [0, host_rows) is skipped and reported as HS_ERR_BAD_INDEX in *status.
+ * ------------------------------------------------------------------------- */
+int hs_backup(const void* src, const int64_t* src_rows, void* host_pool,
+              const int32_t* dst_slots, int32_t n, int64_t row_bytes, int64_t host_rows,
+              int32_t* status, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * S4  hs_sparse_decode -- [PT] 3.1 eqs. (4)-(6) (online softmax over tiles of
+ * the candidate set), 3.2 (mask before the exponent; an empty set gives a
+ * zero output and LSE = -inf) and eq. (7) (split-KV merge); [PA] 1.4 (GQA:
+ * one work unit per KV head serves its query-head group).
+ *
+ * q          bf16 [rows, heads, d_qk].
+ * k_base     bf16: K element (row j, kv head g, dim d) at
+ *            k_base[j * row_stride + g * kv_head_stride + d];  v_base likewise.
+ *            MLA passes k_base == v_base (V = the first d_v columns of the row).
+ *            Both bases 16-byte aligned; row_stride and kv_head_stride
+ *            multiples of 8 elements.
+ * num_kv_rows rows addressable from k_base / v_base; a kv_rows entry outside
+ *            [0, num_kv_rows) is skipped and reported as HS_ERR_BAD_INDEX.
+ * kv_rows    int32 [rows, kv_heads, cap]: candidate rows per (row, kv head);
+ *            -1 entries are skipped.  Taken as given: pass a set (S1 output),
+ *            a repeated row would be weighted twice.
+ * count      int32 [rows, kv_heads] or NULL: entries j >= count are not read.
+ * heads      query heads; heads % kv_heads == 0, head h reads kv head
+ *            h / (heads / kv_heads).
+ * scale      softmax scale (e.g. 1/sqrt(d_qk)).
+ * out        bf16 [rows, heads, d_v] = sum_j softmax_j V_j (fp32 accumulate,
+ *            round to nearest even).
+ * lse        fp32 [rows, heads] natural-log LSE, or NULL.
+ * workspace  device scratch of at least hs_sparse_decode_workspace_bytes(..)
+ *            bytes (split-KV partial states); may be NULL when that is 0.
+ * status     int32 device word or NULL (HS_ERR_TIMEOUT from bounded waits,
+ *            HS_ERR_BAD_INDEX from skipped rows).
+ * Supported shapes: (d_qk, d_v) = (576, 512) with kv_heads == 1 and k_base
+ * == v_base (MLA), or d_qk == d_v == 128 with heads / kv_heads <= 8 (GQA);
+ * others return HS_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------- */
+int64_t hs_sparse_decode_workspace_bytes(int32_t rows, int32_t heads, int32_t kv_heads,
+                                         int32_t cap, int32_t d_qk, int32_t d_v);
+
+int hs_sparse_decode(const void* q, const void* k_base, const void* v_base, int64_t row_stride,
+                     int64_t kv_head_stride, int64_t num_kv_rows, const int32_t* kv_rows,
+                     const int32_t* count,
+                     int32_t rows, int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
+                     int32_t d_v, float scale, void* out, float* lse, void* workspace,
+                     int64_t workspace_bytes, int32_t* status, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hs_merge_states -- [PT] 3.2 eq. (7) / [PA] 1.4 combine, the split-KV merge
+ * used inside hs_sparse_decode, exposed for testing.
+ * m, l       fp32 [n, parts]: per-part maximum logit in log2 units (logit *
+ *            log2 e) and the sum of 2^(s - m); l == 0 marks an empty part.
+ * o          fp32 [n, parts, d_v]: unnormalised sum of 2^(s - m) V.
+ * out        bf16 [n, d_v] = merged o / merged l (0 if every part is empty).
+ * lse        fp32 [n] natural-log LSE (-inf if empty), or NULL.
+ * ------------------------------------------------------------------------- */
+int hs_merge_states(const float* m, const float* l, const float* o, int32_t n, int32_t parts,
+                    int32_t d_v, void* out, float* lse, hs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_API_H */

@@ -1,0 +1,414 @@
+// hs_attention.cu -- S4, sparse decode attention on CUDA cores, and the
+// split-KV merge.
+//
+// PaperTrace 5.1.1 "从索引到 Kernel": section 3.1 eqs. (4)-(6) (per-tile max,
+// exponent sums and rescaled accumulators), section 3.2 (mask before the
+// exponent; an empty candidate set gives a zero output and LSE = -inf) and
+// eq. (7) (exact split-KV merge of unnormalised partial states).
+// "PagedAttention 与 RadixAttention：上游机制与海光实现对照" section 1.4: the
+// exp2 form with scale * log2(e) folded in, the v2 combine, and the GQA grid
+// over KV heads so that one work unit serves its whole query-head group and
+// reads each K/V row once.
+//
+// GB300 design (HBM-bound: ~4 FLOP/byte for GQA): one CTA of 8 warps per
+// (index row, KV head, head chunk, split).  Each warp streams its share of
+// candidate rows straight from the paged cache (no gather copy: PaperTrace
+// section 2.1 eq. (3)), every lane holding one 4-byte bf16 pair of each 64-
+// element block, so a warp-wide load of a row is one coalesced 128-byte line.
+// Warps keep private online-softmax states (eqs. 5-6 in the exp2 domain);
+// the 8 states are merged by eq. (7) through shared memory, and the splits by
+// merge_kernel (eq. 7 again) when a row is split.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include <algorithm>
+
+#include "hs_common.cuh"
+
+namespace hs_attn {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct AttnArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    int64_t row_stride, head_stride, num_kv_rows;
+    const int32_t* kv_rows;
+    const int32_t* count;
+    int32_t rows, cap, heads, kv_heads, d_qk, d_v;
+    float scale_log2;  // scale * log2(e)
+    __nv_bfloat16* out;
+    float* lse;
+    float* part_m;  // [rows*heads, splits]
+    float* part_l;
+    float* part_o;  // [rows*heads, splits, d_v]
+    int32_t splits, chunks_per_kvh;
+    int32_t* status;
+};
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    float2 r;
+    r.x = __uint_as_float(u << 16);
+    r.y = __uint_as_float(u & 0xffff0000u);
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// G query heads of one KV head, rows of DQK (K) / DV (V) bf16 elements.
+template <int DQK, int DV, int G, bool SHARED_KV, int U>
+__global__ void __launch_bounds__(kThreads) attn_cc_kernel(const AttnArgs a) {
+    constexpr int NQ = DQK / 64;
+    constexpr int NV = DV / 64;
+    extern __shared__ __align__(16) float red[];  // [kWarps][G][DV] + m,l [kWarps][G]
+
+    const int unit = blockIdx.x;
+    const int split = blockIdx.y;
+    const int chunk = unit % a.chunks_per_kvh;
+    const int kvh = (unit / a.chunks_per_kvh) % a.kv_heads;
+    const int row = unit / (a.chunks_per_kvh * a.kv_heads);
+    const int group = a.heads / a.kv_heads;
+    const int h0 = kvh * group + chunk * G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Query registers, pre-scaled into the exp2 domain.
+    float2 q[G][NQ];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint32_t* qr =
+            reinterpret_cast<const uint32_t*>(a.q + (int64_t(row) * a.heads + h0 + h) * DQK);
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            float2 f = bf2_to_f2(__ldg(qr + 32 * i + lane));
+            q[h][i] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+        }
+    }
+    float2 o[G][NV];
+    float m[G], l[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -CUDART_INF_F;
+        l[h] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) o[h][i] = make_float2(0.f, 0.f);
+    }
+
+    const int64_t idx_base = (int64_t(row) * a.kv_heads + kvh) * a.cap;
+    const int n = a.count ? min(max(a.count[int64_t(row) * a.kv_heads + kvh], 0), a.cap) : a.cap;
+    const int per = (n + a.splits - 1) / a.splits;
+    const int t0 = min(n, split * per), t1 = min(n, t0 + per);
+    const char* kb = reinterpret_cast<const char*>(a.k) + int64_t(kvh) * a.head_stride * 2;
+    const char* vb = reinterpret_cast<const char*>(a.v) + int64_t(kvh) * a.head_stride * 2;
+    bool bad = false;
+
+    for (int j0 = t0 + warp * U; j0 < t1; j0 += kWarps * U) {
+        int64_t rowsel[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u;
+            int64_t r = j < t1 ? int64_t(__ldg(a.kv_rows + idx_base + j)) : -1;
+            if (r >= a.num_kv_rows) { bad = true; r = -1; }
+            if (r < 0) r = -1;
+            rowsel[u] = r;
+        }
+        uint32_t kr[U][NQ];
+        uint32_t vr[U][SHARED_KV ? 1 : NV];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (rowsel[u] >= 0) {  // warp-uniform branch
+                const uint32_t* kp =
+                    reinterpret_cast<const uint32_t*>(kb + rowsel[u] * a.row_stride * 2);
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) kr[u][i] = __ldg(kp + 32 * i + lane);
+                if constexpr (!SHARED_KV) {
+                    const uint32_t* vp =
+                        reinterpret_cast<const uint32_t*>(vb + rowsel[u] * a.row_stride * 2);
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) vr[u][i] = __ldg(vp + 32 * i + lane);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) kr[u][i] = 0u;
+                if constexpr (!SHARED_KV) {
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) vr[u][i] = 0u;
+                }
+            }
+        }
+        float s[U][G];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) {
+                    const float2 kf = bf2_to_f2(kr[u][i]);
+                    acc = fmaf(q[h][i].x, kf.x, acc);
+                    acc = fmaf(q[h][i].y, kf.y, acc);
+                }
+                acc = warp_sum(acc);
+                s[u][h] = rowsel[u] >= 0 ? acc : -CUDART_INF_F;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float mb = s[0][h];
+#pragma unroll
+            for (int u = 1; u < U; ++u) mb = fmaxf(mb, s[u][h]);
+            const float mn = fmaxf(m[h], mb);
+            if (mn == -CUDART_INF_F) continue;  // nothing valid yet: skip the empty tile
+            const float alpha = exp2f(m[h] - mn);
+            float p[U];
+            float ps = 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                p[u] = exp2f(s[u][h] - mn);
+                ps += p[u];
+            }
+            l[h] = l[h] * alpha + ps;
+            m[h] = mn;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                float2 acc = make_float2(o[h][i].x * alpha, o[h][i].y * alpha);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float2 vf = bf2_to_f2(SHARED_KV ? kr[u][i] : vr[u][SHARED_KV ? 0 : i]);
+                    acc.x = fmaf(p[u], vf.x, acc.x);
+                    acc.y = fmaf(p[u], vf.y, acc.y);
+                }
+                o[h][i] = acc;
+            }
+        }
+    }
+    if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+
+    // Merge the warps' states (eq. 7) through shared memory.
+    float* so = red;                           // [kWarps][G][DV]
+    float* sm = red + kWarps * G * DV;         // [kWarps][G]
+    float* sl = sm + kWarps * G;               // [kWarps][G]
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            float2* dst = reinterpret_cast<float2*>(so + (warp * G + h) * DV + 64 * i) + lane;
+            *dst = o[h][i];
+        }
+        if (lane == 0) {
+            sm[warp * G + h] = m[h];
+            sl[warp * G + h] = l[h];
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * DV; e += kThreads) {
+        const int h = e / DV, d = e % DV;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            if (sl[w * G + h] > 0.f) M = fmaxf(M, sm[w * G + h]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float lw = sl[w * G + h];
+                if (!(lw > 0.f)) continue;
+                const float sc = exp2f(sm[w * G + h] - M);
+                L = fmaf(sc, lw, L);
+                O = fmaf(sc, so[(w * G + h) * DV + d], O);
+            }
+        }
+        const int64_t qh = int64_t(row) * a.heads + h0 + h;
+        if (a.splits == 1) {
+            a.out[qh * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            if (d == 0 && a.lse != nullptr)
+                a.lse[qh] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+        } else {
+            a.part_o[(qh * a.splits + split) * DV + d] = O;
+            if (d == 0) {
+                a.part_m[qh * a.splits + split] = M;
+                a.part_l[qh * a.splits + split] = L;
+            }
+        }
+    }
+}
+
+// Eq. (7) over `parts` partial states per output row; m in log2 units.
+__global__ void merge_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                             const float* __restrict__ po, int32_t parts, int32_t d_v,
+                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    const int64_t n = blockIdx.x;
+    const float* m = pm + n * parts;
+    const float* l = pl + n * parts;
+    float M = -CUDART_INF_F;
+    for (int p = 0; p < parts; ++p)
+        if (l[p] > 0.f) M = fmaxf(M, m[p]);
+    float L = 0.f;
+    if (M != -CUDART_INF_F)
+        for (int p = 0; p < parts; ++p)
+            if (l[p] > 0.f) L = fmaf(exp2f(m[p] - M), l[p], L);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int d = threadIdx.x; d < d_v; d += blockDim.x) {
+        float O = 0.f;
+        if (M != -CUDART_INF_F)
+            for (int p = 0; p < parts; ++p)
+                if (l[p] > 0.f) O = fmaf(exp2f(m[p] - M), po[(n * parts + p) * d_v + d], O);
+        out[n * d_v + d] = __float2bfloat16_rn(O * inv);
+    }
+    if (threadIdx.x == 0 && lse != nullptr)
+        lse[n] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+}
+
+// ----------------------------------------------------------------------------
+// Host side: kernel choice and split policy.
+
+struct Plan {
+    int kind;  // 0 unsupported, 1 MLA (576/512 shared row), 2 GQA d=128
+    int G;     // heads per CTA
+    int chunks_per_kvh;
+    int splits;
+};
+
+Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bool shared) {
+    Plan p{0, 0, 0, 1};
+    if (rows <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads) return p;
+    const int group = heads / kv_heads;
+    if (d_qk == 576 && d_v == 512 && kv_heads == 1 && shared && heads % 4 == 0) {
+        p.kind = 1;
+        p.G = 4;
+    } else if (d_qk == 128 && d_v == 128 && (group == 1 || group == 2 || group == 4 || group == 8)) {
+        p.kind = 2;
+        p.G = group;
+    } else {
+        return p;
+    }
+    p.chunks_per_kvh = group / p.G;
+    const int64_t units = int64_t(rows) * kv_heads * p.chunks_per_kvh;
+    const int64_t target = 2LL * hs_host::num_sms();
+    int64_t s = (target + units - 1) / units;
+    s = hs::min64(s, std::max(1, cap / 32));
+    s = hs::max64(1, hs::min64(s, 64));
+    p.splits = int(s);
+    return p;
+}
+
+int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
+    if (p.kind == 0 || p.splits <= 1) return 0;
+    const int64_t n = int64_t(rows) * heads;
+    return n * p.splits * (2 + int64_t(d_v)) * int64_t(sizeof(float));
+}
+
+template <int DQK, int DV, int G, bool SHARED, int U>
+int launch(const AttnArgs& a, int units, hs_stream_t stream) {
+    auto kern = attn_cc_kernel<DQK, DV, G, SHARED, U>;
+    const size_t smem = size_t(kWarps) * G * (DV + 2) * sizeof(float);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess)
+            return HS_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    dim3 grid(units, a.splits);
+    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return hs_host::launch_status();
+}
+
+}  // namespace hs_attn
+
+using namespace hs_attn;
+
+extern "C" int64_t hs_sparse_decode_workspace_bytes(int32_t rows, int32_t heads,
+                                                    int32_t kv_heads, int32_t cap,
+                                                    int32_t d_qk, int32_t d_v) {
+    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, kv_heads == 1 && d_qk == 576);
+    return workspace_bytes(p, rows, heads, d_v);
+}
+
+extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v_base,
+                                int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
+                                const int32_t* kv_rows, const int32_t* count, int32_t rows,
+                                int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
+                                int32_t d_v, float scale, void* out, float* lse,
+                                void* workspace, int64_t workspace_bytes_given, int32_t* status,
+                                hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || heads <= 0 || kv_heads <= 0 || d_qk <= 0 || d_v <= 0 ||
+        row_stride <= 0 || kv_head_stride < 0 || num_kv_rows < 0)
+        return HS_ERR_INVALID_ARG;
+    if (rows == 0) return HS_OK;
+    if (q == nullptr || k_base == nullptr || v_base == nullptr || out == nullptr ||
+        (cap > 0 && kv_rows == nullptr))
+        return HS_ERR_INVALID_ARG;
+    const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(q) || !al(k_base) || !al(v_base) || !al(out) || row_stride % 8 || kv_head_stride % 8)
+        return HS_ERR_MISALIGNED;
+    const bool shared = k_base == v_base;
+    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, shared);
+    if (p.kind == 0) return HS_ERR_UNSUPPORTED;
+    const int64_t ws = workspace_bytes(p, rows, heads, d_v);
+    if (ws > 0 && (workspace == nullptr || workspace_bytes_given < ws)) return HS_ERR_CAPACITY;
+    AttnArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k_base);
+    a.v = static_cast<const __nv_bfloat16*>(v_base);
+    a.row_stride = row_stride;
+    a.head_stride = kv_head_stride;
+    a.num_kv_rows = num_kv_rows;
+    a.kv_rows = kv_rows;
+    a.count = count;
+    a.rows = rows;
+    a.cap = cap;
+    a.heads = heads;
+    a.kv_heads = kv_heads;
+    a.d_qk = d_qk;
+    a.d_v = d_v;
+    a.scale_log2 = scale * kLog2e;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.splits = p.splits;
+    a.chunks_per_kvh = p.chunks_per_kvh;
+    a.status = status;
+    const int64_t n = int64_t(rows) * heads;
+    if (p.splits > 1) {
+        float* w = static_cast<float*>(workspace);
+        a.part_m = w;
+        a.part_l = w + n * p.splits;
+        a.part_o = w + 2 * n * p.splits;
+    }
+    const int units = rows * kv_heads * p.chunks_per_kvh;
+    int rc;
+    if (p.kind == 1) {
+        rc = launch<576, 512, 4, true, 2>(a, units, stream);
+    } else {
+        switch (p.G) {
+            case 1: rc = launch<128, 128, 1, false, 4>(a, units, stream); break;
+            case 2: rc = launch<128, 128, 2, false, 4>(a, units, stream); break;
+            case 4: rc = launch<128, 128, 4, false, 4>(a, units, stream); break;
+            default: rc = launch<128, 128, 8, false, 2>(a, units, stream); break;
+        }
+    }
+    if (rc != HS_OK || p.splits == 1) return rc;
+    merge_kernel<<<int(n), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        a.part_m, a.part_l, a.part_o, p.splits, d_v, a.out, lse);
+    return hs_host::launch_status();
+}
+
+extern "C" int hs_merge_states(const float* m, const float* l, const float* o, int32_t n,
+                               int32_t parts, int32_t d_v, void* out, float* lse,
+                               hs_stream_t stream) {
+    if (n < 0 || parts <= 0 || d_v <= 0) return HS_ERR_INVALID_ARG;
+    if (n == 0) return HS_OK;
+    if (m == nullptr || l == nullptr || o == nullptr || out == nullptr) return HS_ERR_INVALID_ARG;
+    merge_kernel<<<n, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        m, l, o, parts, d_v, static_cast<__nv_bfloat16*>(out), lse);
+    return hs_host::launch_status();
+}

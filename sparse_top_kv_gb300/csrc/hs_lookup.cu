@@ -1,0 +1,284 @@
+// hs_lookup.cu -- S2, hot-buffer lookup keyed by global slot id, with the
+// deterministic LRU slot assignment of the vLLM HiSparse walkthrough
+// (hisparse_swap_in_kernel, Phase 1 .. Phase 4), and the state reset
+// ("Hisparse hot cache初始化": zero-initialised buffer, recycled slots
+// invalidated before reuse).
+//
+// GB300 design: one 1024-thread CTA per request row.  Phase 1 builds an
+// open-addressing hash of the row's pending slot ids in shared memory; the
+// first occurrence of a repeated id is kept with atomicMin on its position,
+// so repeats resolve deterministically (the walkthrough's hash overwrites on
+// a repeated key, which is racy).  Phase 2 walks the LRU list in 1024-wide
+// chunks; hits and evictables are compacted in LRU order by a block-wide
+// ballot/popc/shuffle scan.  Phase 3 ranks the misses in row order with the
+// same scan and hands them E[0], E[1], ...  Phase 4 writes
+// E[M:] ++ E[:M] ++ hits.  The output is bit-identical to the sequential
+// definition for every thread schedule.
+#include "hs_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int32_t kEmpty = -1;
+constexpr int32_t kDone = INT32_MIN;
+constexpr int kMaxSmem = 227 * 1024;
+
+struct LookupArgs {
+    const int32_t* slot;
+    const int32_t* count;
+    int32_t rows, cap, num_real_rows;
+    const int32_t* newest_slot;
+    int32_t* dgi;
+    int16_t* lru;
+    int32_t hot_size;
+    int64_t region_stride;
+    int32_t* hot_idx;
+    uint8_t* miss_mask;
+    int32_t* miss_src;
+    int64_t* miss_dst;
+    int32_t* miss_count;
+    int64_t* stats;
+    int32_t* err;
+    int32_t hash_log2;
+};
+
+__device__ __forceinline__ uint32_t hash_of(int32_t g, int log2n) {
+    return (uint32_t(g) * 2654435761u) >> (32 - log2n);
+}
+
+// Position of key g in the table, or -1 when absent.
+__device__ __forceinline__ int find_key(const int32_t* keys, int32_t g, int log2n) {
+    const uint32_t mask = (1u << log2n) - 1u;
+    uint32_t h = hash_of(g, log2n);
+    for (uint32_t probe = 0; probe <= mask; ++probe) {
+        const int32_t k = keys[h];
+        if (k == g) return int(h);
+        if (k == kEmpty) return -1;
+        h = (h + 1u) & mask;
+    }
+    return -1;
+}
+
+__global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int scan_scratch[33];
+    __shared__ int s_dup;
+
+    const int HS = 1 << a.hash_log2;
+    int32_t* keys = reinterpret_cast<int32_t*>(smem);
+    int32_t* vals = keys + HS;
+    int32_t* state = vals + HS;
+    int16_t* E = reinterpret_cast<int16_t*>(state + a.cap);
+    int16_t* H = E + a.hot_size;
+
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int cap = a.cap;
+    const int hot_size = a.hot_size;
+    const int32_t* g_row = a.slot + int64_t(row) * cap;
+    int32_t* out = a.hot_idx + int64_t(row) * cap;
+    uint8_t* mm = a.miss_mask ? a.miss_mask + int64_t(row) * cap : nullptr;
+    int32_t* msrc = a.miss_src + int64_t(row) * cap;
+    int64_t* mdst = a.miss_dst + int64_t(row) * cap;
+
+    if (row >= a.num_real_rows) {  // CUDA-graph padding row
+        for (int i = tid; i < cap; i += kThreads) {
+            out[i] = -1;
+            if (mm) mm[i] = 0;
+            msrc[i] = -1;
+            mdst[i] = -1;
+        }
+        if (tid == 0) {
+            a.miss_count[row] = 0;
+            a.err[row] = 0;
+        }
+        return;
+    }
+    int32_t* dgi = a.dgi + int64_t(row) * hot_size;
+    int16_t* lru = a.lru + int64_t(row) * hot_size;
+    const int64_t hot_base = int64_t(row) * a.region_stride;
+
+    for (int h = tid; h < HS; h += kThreads) {
+        keys[h] = kEmpty;
+        vals[h] = INT32_MAX;
+    }
+    if (tid == 0) s_dup = 0;
+    __syncthreads();
+
+    const int n = a.count ? min(max(a.count[row], 0), cap) : cap;
+    const int32_t newest = a.newest_slot ? a.newest_slot[row] : -1;
+
+    // Phase 1: classify entries, hash the pending ids (first occurrence wins).
+    const uint32_t hmask = uint32_t(HS) - 1u;
+    for (int i = tid; i < cap; i += kThreads) {
+        const int32_t g = i < n ? g_row[i] : -1;
+        if (mm) mm[i] = 0;
+        msrc[i] = -1;
+        mdst[i] = -1;
+        if (g < 0) {
+            out[i] = -1;
+            state[i] = kDone;
+        } else if (newest >= 0 && g == newest) {
+            out[i] = int32_t(hot_base + hot_size);
+            state[i] = kDone;
+        } else {
+            uint32_t h = hash_of(g, a.hash_log2);
+            for (uint32_t probe = 0; probe <= hmask; ++probe) {
+                const int32_t old = atomicCAS(&keys[h], kEmpty, g);
+                if (old == kEmpty || old == g) {
+                    atomicMin(&vals[h], i);
+                    break;
+                }
+                h = (h + 1u) & hmask;
+            }
+            state[i] = g;
+        }
+    }
+    __syncthreads();
+    // Repeats of an earlier pending id resolve to -1.
+    {
+        int dups = 0;
+        for (int i = tid; i < cap; i += kThreads) {
+            const int32_t g = state[i];
+            if (g == kDone) continue;
+            const int h = find_key(keys, g, a.hash_log2);
+            if (h >= 0 && vals[h] != i) {
+                state[i] = kDone;
+                out[i] = -1;
+                ++dups;
+            }
+        }
+        if (dups) atomicAdd(&s_dup, dups);
+    }
+    __syncthreads();
+
+    // Phase 2: LRU walk, least -> most recently used.
+    int hits_total = 0;
+    for (int base = 0; base < hot_size; base += kThreads) {
+        const int pos = base + tid;
+        int hit = 0;
+        int16_t s = -1;
+        if (pos < hot_size) {
+            s = lru[pos];
+            if (s >= 0 && s < hot_size) {
+                const int32_t cg = dgi[s];
+                if (cg >= 0) {
+                    const int h = find_key(keys, cg, a.hash_log2);
+                    if (h >= 0) {
+                        const int i = vals[h];
+                        out[i] = int32_t(hot_base + s);
+                        state[i] = kDone;
+                        hit = 1;
+                    }
+                }
+            }
+        }
+        int tot;
+        const int excl = hs::block_excl_scan(hit, scan_scratch, &tot);
+        if (pos < hot_size) {
+            if (hit) H[hits_total + excl] = s;
+            else E[pos - (hits_total + excl)] = s;
+        }
+        hits_total += tot;
+    }
+    const int nE = hot_size - hits_total;
+
+    // Phase 3: misses in row order take E[0], E[1], ...
+    int miss_total = 0;
+    for (int base = 0; base < cap; base += kThreads) {
+        const int i = base + tid;
+        const int32_t g = i < cap ? state[i] : kDone;
+        const int is_miss = g != kDone;
+        int tot;
+        const int excl = hs::block_excl_scan(is_miss, scan_scratch, &tot);
+        if (is_miss) {
+            const int m = miss_total + excl;
+            const int16_t s = m < nE ? E[m] : int16_t(-1);
+            if (s >= 0 && s < hot_size) {
+                out[i] = int32_t(hot_base + s);
+                if (mm) mm[i] = 1;
+                dgi[s] = g;
+                msrc[m] = g;
+                mdst[m] = hot_base + s;
+            } else {
+                out[i] = -1;  // only reachable with a corrupted LRU list
+            }
+        }
+        miss_total += tot;
+    }
+    const int M = min(miss_total, nE);
+
+    // Phase 4: new LRU order = E[M:] ++ E[:M] ++ hits.
+    for (int j = tid; j < hot_size; j += kThreads) {
+        int16_t s;
+        if (j < nE - M) s = E[M + j];
+        else if (j < nE) s = E[j - (nE - M)];
+        else s = H[j - nE];
+        lru[j] = s;
+    }
+    if (tid == 0) {
+        a.miss_count[row] = M;
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.stats),
+                  static_cast<unsigned long long>(hits_total));
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + 1),
+                  static_cast<unsigned long long>(M));
+        a.err[row] = s_dup;
+    }
+}
+
+__global__ void reset_kernel(int32_t* dgi, int16_t* lru, int32_t hot_size) {
+    const int64_t base = int64_t(blockIdx.x) * hot_size;
+    for (int j = threadIdx.x; j < hot_size; j += blockDim.x) {
+        dgi[base + j] = -1;
+        lru[base + j] = int16_t(j);
+    }
+}
+
+}  // namespace
+
+extern "C" int hs_hot_state_reset(int32_t* dgi, int16_t* lru, int32_t rows, int32_t hot_size,
+                                  hs_stream_t stream) {
+    if (rows < 0 || hot_size <= 0 || hot_size > 32767) return HS_ERR_INVALID_ARG;
+    if (rows == 0) return HS_OK;
+    if (dgi == nullptr || lru == nullptr) return HS_ERR_INVALID_ARG;
+    reset_kernel<<<rows, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dgi, lru, hot_size);
+    return hs_host::launch_status();
+}
+
+extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows,
+                                    int32_t cap, int32_t num_real_rows,
+                                    const int32_t* newest_slot, int32_t* dgi, int16_t* lru,
+                                    int32_t hot_size, int64_t region_stride, int32_t* hot_idx,
+                                    uint8_t* miss_mask, int32_t* miss_src, int64_t* miss_dst,
+                                    int32_t* miss_count, int64_t* stats, int32_t* err,
+                                    hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || hot_size <= 0 || hot_size > 32767 || num_real_rows < 0)
+        return HS_ERR_INVALID_ARG;
+    if (region_stride < int64_t(hot_size) + 1) return HS_ERR_INVALID_ARG;
+    if (int64_t(rows) * region_stride > INT32_MAX) return HS_ERR_INVALID_ARG;
+    if (cap > hot_size) return HS_ERR_CAPACITY;
+    if (rows == 0) return HS_OK;
+    if ((cap > 0 && slot == nullptr) || dgi == nullptr || lru == nullptr ||
+        (cap > 0 && (hot_idx == nullptr || miss_src == nullptr || miss_dst == nullptr)) ||
+        miss_count == nullptr || stats == nullptr || err == nullptr)
+        return HS_ERR_INVALID_ARG;
+    int log2n = 6;
+    while ((1 << log2n) < 2 * cap) ++log2n;
+    const size_t smem = size_t(8) * (size_t(1) << log2n) + size_t(4) * cap +
+                        size_t(4) * hot_size;
+    if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxSmem) != cudaSuccess)
+            return HS_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    LookupArgs a{slot,     count,    rows,     cap,        num_real_rows, newest_slot,
+                 dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
+                 miss_src, miss_dst, miss_count, stats,    err,           log2n};
+    lookup_kernel<<<rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return hs_host::launch_status();
+}

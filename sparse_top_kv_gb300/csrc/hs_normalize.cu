@@ -1,0 +1,200 @@
+// hs_normalize.cu -- S1, candidate normalisation.
+//
+// PaperTrace 5.1.1 "从索引到 Kernel": section 1.1 eq. (1) S = unique(D u W u A)
+// with range, causality and batch-ownership checks; section 1.2 eq. (2)
+// b = floor(t / B) and the block-table lookup; section 7.3 eq. (16) (set
+// semantics: membership by logical t, output ordered by t).  vLLM HiSparse
+// walkthrough, "_convert_req_index_to_global_index_kernel": slot = table[b] *
+// B + t mod B, invalid tokens propagate as -1.
+//
+// GB300 design: one CTA per index row.  Membership is a bitmap over the
+// row's positions in shared memory (a counting sort): W u A and then D are
+// set with atomicOr (the returned old word tells a duplicate), and the
+// ascending, de-duplicated output comes from a block-wide scan of the
+// bitmap words' popcounts (warp shuffles + ballot-free popc).  The result is
+// exactly the set definition, whatever the thread schedule.  Contexts longer
+// than one bitmap window are processed in successive windows of kWindowBits
+// positions.
+#include "hs_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWordsPerThread = 8;
+constexpr int kWindowWords = kThreads * kWordsPerThread;     // 4096 words = 16 KB
+constexpr int64_t kWindowBits = int64_t(kWindowWords) * 32;  // 131072 positions
+
+struct NormArgs {
+    const int32_t* cand;
+    int32_t rows, n_cand, window, num_sinks;
+    const int32_t* row_req;
+    const int32_t* seq_lens;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int32_t max_blocks;
+    const int32_t* page_owner;
+    int32_t num_reqs, num_pages, page_size, cap;
+    int32_t* out_tok;
+    int32_t* out_slot;
+    int32_t* out_count;
+    int32_t* err_counts;
+};
+
+// Checks of a position already known to satisfy 0 <= t < T.
+// Returns -1 when valid, else the rejection category (0 range, 2 owner).
+__device__ __forceinline__ int classify_in_range(int64_t t, const int32_t* table,
+                                                 const NormArgs& a, int32_t req) {
+    const int64_t b = t / a.page_size;
+    if (b >= a.max_blocks) return 0;
+    const int32_t p = __ldg(table + b);
+    if (p < 0 || p >= a.num_pages) return 0;
+    if (a.page_owner != nullptr && __ldg(a.page_owner + p) != req) return 2;
+    return -1;
+}
+
+__global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
+    __shared__ uint32_t bm[kWindowWords];
+    __shared__ int scan_scratch[33];
+    __shared__ int s_err[4];
+
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int32_t* cand = a.cand + int64_t(row) * a.n_cand;
+    int32_t* otok = a.out_tok + int64_t(row) * a.cap;
+    int32_t* oslot = a.out_slot + int64_t(row) * a.cap;
+    if (tid < 4) s_err[tid] = 0;
+    __syncthreads();
+
+    const int32_t req = a.row_req[row];
+    int out_n = 0;
+    if (req < 0 || req >= a.num_reqs) {
+        // No request: each dynamic candidate is a range error.
+        int bad = 0;
+        for (int i = tid; i < a.n_cand; i += kThreads) bad += (cand[i] != -1);
+        if (bad) atomicAdd(&s_err[0], bad);
+    } else {
+        const int64_t T = max(a.seq_lens[req], 0);
+        const int32_t* table = a.block_table + int64_t(req) * a.bt_stride;
+        const int64_t a_hi = hs::min64(a.num_sinks, T);        // sinks  [0, a_hi)
+        const int64_t s2 = hs::max64(hs::max64(T - a.window, 0), a_hi);  // window [s2, T)
+
+        // Dynamic candidates outside [0, T) are rejected once, before the windows.
+        {
+            int er = 0, ec = 0;
+            for (int i = tid; i < a.n_cand; i += kThreads) {
+                const int32_t t = cand[i];
+                if (t == -1) continue;
+                if (t < 0) ++er;
+                else if (t >= T) ++ec;
+            }
+            if (er) atomicAdd(&s_err[0], er);
+            if (ec) atomicAdd(&s_err[1], ec);
+        }
+
+        for (int64_t lo = 0; lo < T; lo += kWindowBits) {
+            const int64_t hi = hs::min64(T, lo + kWindowBits);
+            const int nw = int((hi - lo + 31) >> 5);
+            for (int w = tid; w < nw; w += kThreads) bm[w] = 0u;
+            __syncthreads();
+
+            int er = 0, eo = 0, ed = 0;
+            // Structural candidates: sinks [0, a_hi) and window [s2, T) (disjoint).
+            for (int pass = 0; pass < 2; ++pass) {
+                const int64_t b0 = pass == 0 ? hs::max64(lo, 0) : hs::max64(lo, s2);
+                const int64_t b1 = pass == 0 ? hs::min64(hi, a_hi) : hs::min64(hi, T);
+                for (int64_t t = b0 + tid; t < b1; t += kThreads) {
+                    const int c = classify_in_range(t, table, a, req);
+                    if (c < 0) {
+                        const int64_t o = t - lo;
+                        atomicOr(&bm[o >> 5], 1u << (o & 31));
+                    } else if (c == 0) {
+                        ++er;
+                    } else {
+                        ++eo;
+                    }
+                }
+            }
+            __syncthreads();
+            // Dynamic candidates inside this window.
+            for (int i = tid; i < a.n_cand; i += kThreads) {
+                const int64_t t = cand[i];
+                if (t < lo || t >= hi) continue;
+                const int c = classify_in_range(t, table, a, req);
+                if (c == 0) { ++er; continue; }
+                if (c == 2) { ++eo; continue; }
+                const int64_t o = t - lo;
+                const uint32_t bit = 1u << (o & 31);
+                const uint32_t old = atomicOr(&bm[o >> 5], bit);
+                if (old & bit) ++ed;
+            }
+            if (er) atomicAdd(&s_err[0], er);
+            if (eo) atomicAdd(&s_err[2], eo);
+            if (ed) atomicAdd(&s_err[3], ed);
+            __syncthreads();
+
+            // Ascending compaction of the window.
+            uint32_t words[kWordsPerThread];
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < kWordsPerThread; ++k) {
+                const int w = tid * kWordsPerThread + k;
+                words[k] = w < nw ? bm[w] : 0u;
+                cnt += __popc(words[k]);
+            }
+            int total;
+            int pos = out_n + hs::block_excl_scan(cnt, scan_scratch, &total);
+#pragma unroll
+            for (int k = 0; k < kWordsPerThread; ++k) {
+                uint32_t x = words[k];
+                const int64_t base = lo + int64_t(tid * kWordsPerThread + k) * 32;
+                while (x) {
+                    const int b = __ffs(x) - 1;
+                    x &= x - 1;
+                    const int64_t t = base + b;
+                    const int64_t p = __ldg(table + t / a.page_size);
+                    otok[pos] = int32_t(t);
+                    oslot[pos] = int32_t(p * a.page_size + t % a.page_size);
+                    ++pos;
+                }
+            }
+            out_n += total;
+            __syncthreads();
+        }
+    }
+    for (int j = out_n + tid; j < a.cap; j += kThreads) {
+        otok[j] = -1;
+        oslot[j] = -1;
+    }
+    __syncthreads();
+    if (tid == 0) a.out_count[row] = out_n;
+    if (tid < 4) a.err_counts[int64_t(row) * 4 + tid] = s_err[tid];
+}
+
+}  // namespace
+
+extern "C" int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n_cand,
+                                    int32_t window, int32_t num_sinks, const int32_t* row_req,
+                                    const int32_t* seq_lens, const int32_t* block_table,
+                                    int64_t bt_stride, int32_t max_blocks,
+                                    const int32_t* page_owner, int32_t num_reqs,
+                                    int32_t num_pages, int32_t page_size, int32_t cap,
+                                    int32_t* out_tok, int32_t* out_slot, int32_t* out_count,
+                                    int32_t* err_counts, hs_stream_t stream) {
+    if (rows < 0 || n_cand < 0 || window < 0 || num_sinks < 0 || max_blocks < 0 ||
+        num_reqs < 0 || num_pages < 0 || page_size <= 0 || cap < 0 || bt_stride < max_blocks)
+        return HS_ERR_INVALID_ARG;
+    if (int64_t(cap) < int64_t(n_cand) + window + num_sinks) return HS_ERR_CAPACITY;
+    if (int64_t(num_pages) * page_size > INT32_MAX) return HS_ERR_INVALID_ARG;
+    if (rows == 0) return HS_OK;
+    if ((n_cand > 0 && cand == nullptr) || row_req == nullptr || out_tok == nullptr ||
+        out_slot == nullptr || out_count == nullptr || err_counts == nullptr)
+        return HS_ERR_INVALID_ARG;
+    if (num_reqs > 0 && (seq_lens == nullptr || (max_blocks > 0 && block_table == nullptr)))
+        return HS_ERR_INVALID_ARG;
+    NormArgs a{cand,      rows,      n_cand,     window,    num_sinks, row_req,
+               seq_lens,  block_table, bt_stride, max_blocks, page_owner, num_reqs,
+               num_pages, page_size, cap,        out_tok,   out_slot,  out_count,
+               err_counts};
+    normalize_kernel<<<rows, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return hs_host::launch_status();
+}

@@ -1,0 +1,237 @@
+"""Thin Python binding of libhs (include/hs_api.h), same names as the C ABI.
+
+Argument marshalling only: checks dtypes/devices, allocates output tensors
+when the caller does not pass them, and forwards raw pointers plus the current
+CUDA stream.  Every step of the path runs in the CUDA kernels of libhs.so;
+there is no CPU fallback.  If the library cannot be loaded this module raises.
+"""
+import ctypes
+
+import torch
+
+from . import _build
+
+_lib = None
+
+HS_OK = 0
+STATUS_NAMES = {0: "HS_OK", 1: "HS_ERR_INVALID_ARG", 2: "HS_ERR_MISALIGNED", 3: "HS_ERR_CAPACITY",
+                4: "HS_ERR_CUDA", 5: "HS_ERR_TIMEOUT", 6: "HS_ERR_BAD_INDEX",
+                7: "HS_ERR_UNSUPPORTED"}
+
+
+class HSError(RuntimeError):
+    def __init__(self, name, code):
+        super().__init__(f"{name} failed: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F32 = ctypes.c_float
+
+_SIGS = {
+    "hs_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "hs_host_device_pointer": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
+    "hs_normalize_indices": ([_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _I32, _P, _I32, _I32,
+                              _I32, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
+    "hs_hot_state_reset": ([_P, _P, _I32, _I32, _P], ctypes.c_int),
+    "hs_hot_lookup_assign": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
+                              _P, _P, _P, _P], ctypes.c_int),
+    "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _P, _P],
+                   ctypes.c_int),
+    "hs_backup": ([_P, _P, _P, _P, _I32, _I64, _I64, _P, _P], ctypes.c_int),
+    "hs_sparse_decode_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32], _I64),
+    "hs_sparse_decode": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                          _I32, _F32, _P, _P, _P, _I64, _P, _P], ctypes.c_int),
+    "hs_merge_states": ([_P, _P, _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+}
+
+EXPORTS = tuple(_SIGS)
+
+
+def lib_path():
+    return _build.LIB
+
+
+def lib():
+    """Load libhs.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _call(name, *args):
+    rc = getattr(lib(), name)(*args)
+    if rc != HS_OK:
+        raise HSError(name, rc)
+
+
+def _check(t, dtype, name, cuda=True):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def status_string(code):
+    return lib().hs_status_string(code).decode()
+
+
+def host_device_pointer(t):
+    """Device-visible address of a pinned host tensor."""
+    if not t.is_pinned():
+        raise ValueError("host pool must be pinned (pin_memory())")
+    out = ctypes.c_void_p()
+    _call("hs_host_device_pointer", ctypes.c_void_p(t.data_ptr()), ctypes.byref(out))
+    return out.value
+
+
+# ---------------------------------------------------------------------------
+def normalize_indices(cand, row_req, seq_lens, block_table, page_size, *, window=0, num_sinks=0,
+                      page_owner=None, num_pages, max_blocks=None, cap=None, out=None,
+                      stream=None):
+    """S1.  Returns (tok, slot, count, err) int32 tensors."""
+    for t, n in ((cand, "cand"), (row_req, "row_req"), (seq_lens, "seq_lens"),
+                 (block_table, "block_table"), (page_owner, "page_owner")):
+        _check(t, torch.int32, n)
+    rows, n_cand = cand.shape
+    num_reqs, bt_stride = block_table.shape
+    max_blocks = bt_stride if max_blocks is None else max_blocks
+    cap = n_cand + window + num_sinks if cap is None else cap
+    if out is None:
+        dev = cand.device
+        out = (torch.empty(rows, cap, dtype=torch.int32, device=dev),
+               torch.empty(rows, cap, dtype=torch.int32, device=dev),
+               torch.empty(rows, dtype=torch.int32, device=dev),
+               torch.empty(rows, 4, dtype=torch.int32, device=dev))
+    tok, slot, count, err = out
+    _call("hs_normalize_indices", _ptr(cand), rows, n_cand, window, num_sinks, _ptr(row_req),
+          _ptr(seq_lens), _ptr(block_table), bt_stride, max_blocks, _ptr(page_owner), num_reqs,
+          num_pages, page_size, cap, _ptr(tok), _ptr(slot), _ptr(count), _ptr(err),
+          _stream(stream))
+    return tok, slot, count, err
+
+
+def hot_state_reset(dgi, lru, stream=None):
+    _check(dgi, torch.int32, "dgi")
+    _check(lru, torch.int16, "lru")
+    rows, hot_size = dgi.shape
+    _call("hs_hot_state_reset", _ptr(dgi), _ptr(lru), rows, hot_size, _stream(stream))
+
+
+def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, *,
+                      num_real_rows=None, out=None, with_mask=True, stream=None):
+    """S2.  dgi/lru are updated in place; stats int64 [2] accumulates.
+    Returns (hot_idx, miss_mask, miss_src, miss_dst, miss_count, err)."""
+    _check(slot, torch.int32, "slot")
+    _check(count, torch.int32, "count")
+    _check(newest_slot, torch.int32, "newest_slot")
+    _check(dgi, torch.int32, "dgi")
+    _check(lru, torch.int16, "lru")
+    _check(stats, torch.int64, "stats")
+    rows, cap = slot.shape
+    hot_size = dgi.shape[1]
+    if out is None:
+        dev = slot.device
+        out = (torch.empty(rows, cap, dtype=torch.int32, device=dev),
+               torch.empty(rows, cap, dtype=torch.uint8, device=dev) if with_mask else None,
+               torch.empty(rows, cap, dtype=torch.int32, device=dev),
+               torch.empty(rows, cap, dtype=torch.int64, device=dev),
+               torch.empty(rows, dtype=torch.int32, device=dev),
+               torch.empty(rows, dtype=torch.int32, device=dev))
+    hot_idx, miss_mask, miss_src, miss_dst, miss_count, err = out
+    nrr = rows if num_real_rows is None else num_real_rows
+    _call("hs_hot_lookup_assign", _ptr(slot), _ptr(count), rows, cap, nrr, _ptr(newest_slot),
+          _ptr(dgi), _ptr(lru), hot_size, region_stride, _ptr(hot_idx), _ptr(miss_mask),
+          _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), _ptr(stats), _ptr(err),
+          _stream(stream))
+    return out
+
+
+def swap_in(host_pool_dev, host_rows, hot, row_bytes, miss_src, miss_dst, miss_count, *,
+            dgi=None, hot_size=0, region_stride=0, status=None, stream=None):
+    """S3 SwapIn.  host_pool_dev: device-visible address (int) of the pinned pool."""
+    _check(miss_src, torch.int32, "miss_src")
+    _check(miss_dst, torch.int64, "miss_dst")
+    _check(miss_count, torch.int32, "miss_count")
+    _check(dgi, torch.int32, "dgi")
+    _check(status, torch.int32, "status")
+    rows, cap = miss_src.shape
+    _call("hs_swap_in", ctypes.c_void_p(host_pool_dev), host_rows, _ptr(hot), row_bytes,
+          _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), rows, cap, _ptr(dgi), hot_size,
+          region_stride, _ptr(status), _stream(stream))
+
+
+def backup(src, src_rows, host_pool_dev, dst_slots, row_bytes, host_rows, *, status=None,
+           stream=None):
+    """BackUp: host_pool[dst_slots[i]] = src[src_rows[i]]."""
+    _check(src_rows, torch.int64, "src_rows")
+    _check(dst_slots, torch.int32, "dst_slots")
+    _check(status, torch.int32, "status")
+    _call("hs_backup", _ptr(src), _ptr(src_rows), ctypes.c_void_p(host_pool_dev),
+          _ptr(dst_slots), dst_slots.numel(), row_bytes, host_rows, _ptr(status),
+          _stream(stream))
+
+
+def sparse_decode_workspace_bytes(rows, heads, kv_heads, cap, d_qk, d_v):
+    return int(lib().hs_sparse_decode_workspace_bytes(rows, heads, kv_heads, cap, d_qk, d_v))
+
+
+def sparse_decode(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
+                  scale, d_v, *, out=None, lse=None, workspace=None, status=None, stream=None):
+    """S4.  q bf16 [rows, heads, d_qk]; kv_rows int32 [rows, kv_heads, cap];
+    count int32 [rows, kv_heads] or None.  Returns (out bf16, lse fp32)."""
+    _check(q, torch.bfloat16, "q")
+    _check(kv_rows, torch.int32, "kv_rows")
+    _check(count, torch.int32, "count")
+    _check(status, torch.int32, "status")
+    rows, heads, d_qk = q.shape
+    _, kv_heads, cap = kv_rows.shape
+    if out is None:
+        out = torch.empty(rows, heads, d_v, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=q.device)
+    ws = sparse_decode_workspace_bytes(rows, heads, kv_heads, cap, d_qk, d_v)
+    if ws > 0 and (workspace is None or workspace.numel() * workspace.element_size() < ws):
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
+    _call("hs_sparse_decode", _ptr(q), _ptr(k_base), _ptr(v_base), row_stride, kv_head_stride,
+          num_kv_rows, _ptr(kv_rows), _ptr(count), rows, cap, heads, kv_heads, d_qk, d_v,
+          float(scale), _ptr(out), _ptr(lse), _ptr(workspace) if ws > 0 else None,
+          workspace.numel() * workspace.element_size() if (ws > 0) else 0, _ptr(status),
+          _stream(stream))
+    return out, lse
+
+
+def merge_states(m, l, o, *, out=None, lse=None, stream=None):
+    """Eq. (7) merge: m, l fp32 [n, parts] (m in log2 units); o fp32 [n, parts, d_v]."""
+    for t, n in ((m, "m"), (l, "l"), (o, "o")):
+        _check(t, torch.float32, n)
+    n, parts, d_v = o.shape
+    if out is None:
+        out = torch.empty(n, d_v, dtype=torch.bfloat16, device=o.device)
+    if lse is None:
+        lse = torch.empty(n, dtype=torch.float32, device=o.device)
+    _call("hs_merge_states", _ptr(m), _ptr(l), _ptr(o), n, parts, d_v, _ptr(out), _ptr(lse),
+          _stream(stream))
+    return out, lse

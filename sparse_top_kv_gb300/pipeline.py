@@ -1,0 +1,106 @@
+"""One HiSparse decode step on the GPU, through the C ABI of libhs.
+
+Stage order per step (vLLM HiSparse walkthrough, "swap_in 方法流程详解" and the
+BackUp interface of its overview):
+  (model)  the new token's KV row lands in the request's reserved hot row
+  S1       hs_normalize_indices  candidates -> sorted unique slots
+  S2       hs_hot_lookup_assign  hot rows, misses, LRU update
+  S3       hs_swap_in            missed rows host -> hot;  hs_backup  reserved row -> host
+  S4       hs_sparse_decode      attention over the hot rows
+Torch provides device memory, pinned host memory and the stream; every stage is
+a libhs kernel.
+"""
+import torch
+
+from . import hs
+
+
+class HiSparseDecoder:
+    """Per-layer hot buffer of `num_reqs` regions of `region_stride` rows of
+    `row_width` bf16 elements, backed by a pinned host pool (the only
+    full-size store, keyed by global slot id)."""
+
+    def __init__(self, *, host_pool, block_table, num_pages, page_size, top_k, hot_size,
+                 region_stride, heads, d_qk=576, d_v=512, scale, window=0, num_sinks=0,
+                 device="cuda"):
+        if not host_pool.is_pinned():
+            raise ValueError("host pool must be pinned")
+        self.device = torch.device(device)
+        self.num_reqs = block_table.shape[0]
+        self.row_width = host_pool.shape[1]
+        self.row_bytes = self.row_width * host_pool.element_size()
+        self.host_pool = host_pool
+        self.host_rows = host_pool.shape[0]
+        self.host_dev = hs.host_device_pointer(host_pool)
+        self.block_table = block_table.to(self.device, torch.int32).contiguous()
+        self.num_pages, self.page_size = num_pages, page_size
+        self.top_k, self.hot_size, self.region_stride = top_k, hot_size, region_stride
+        self.heads, self.d_qk, self.d_v, self.scale = heads, d_qk, d_v, scale
+        self.window, self.num_sinks = window, num_sinks
+        R = self.num_reqs
+        dev = self.device
+        self.hot = torch.zeros(R * region_stride, self.row_width, dtype=host_pool.dtype, device=dev)
+        self.dgi = torch.empty(R, hot_size, dtype=torch.int32, device=dev)
+        self.lru = torch.empty(R, hot_size, dtype=torch.int16, device=dev)
+        hs.hot_state_reset(self.dgi, self.lru)
+        self.stats = torch.zeros(2, dtype=torch.int64, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.row_req = torch.arange(R, dtype=torch.int32, device=dev)
+        self.reserved_rows = (torch.arange(R, dtype=torch.int64, device=dev) * region_stride
+                              + hot_size)
+        cap = top_k + window + num_sinks
+        self.cap = cap
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.s1_out = (torch.empty(R, cap, **i32), torch.empty(R, cap, **i32),
+                       torch.empty(R, **i32), torch.empty(R, 4, **i32))
+        self.s2_out = (torch.empty(R, cap, **i32),
+                       torch.empty(R, cap, dtype=torch.uint8, device=dev),
+                       torch.empty(R, cap, **i32),
+                       torch.empty(R, cap, dtype=torch.int64, device=dev),
+                       torch.empty(R, **i32), torch.empty(R, **i32))
+        self.out = torch.empty(R, heads, d_v, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(R, heads, dtype=torch.float32, device=dev)
+        ws = hs.sparse_decode_workspace_bytes(R, heads, 1, cap, d_qk, d_v)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def newest_slots(self, newest_pos, seq_lens):
+        """Slot mapping of the newest positions, int32 [R] (S1 on one candidate)."""
+        tok, slot, count, err = hs.normalize_indices(
+            newest_pos.view(-1, 1), self.row_req, seq_lens, self.block_table, self.page_size,
+            num_pages=self.num_pages)
+        return slot.view(-1).clone()
+
+    def step(self, cand, seq_lens, newest_slot, new_row, q, stream=None):
+        """cand int32 [R, top_k] positions; seq_lens int32 [R]; newest_slot int32
+        [R]; new_row [R, row_width] (the new token's KV row); q bf16 [R, H, d_qk].
+        Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated."""
+        R = self.num_reqs
+        # The model's KV write of the newest token (stand-in): reserved hot rows.
+        self.hot.index_copy_(0, self.reserved_rows, new_row)
+        tok, slot, count, err = hs.normalize_indices(
+            cand, self.row_req, seq_lens, self.block_table, self.page_size,
+            window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
+            out=self.s1_out, stream=stream)
+        hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr = hs.hot_lookup_assign(
+            slot, count, newest_slot, self.dgi, self.lru, self.region_stride, self.stats,
+            out=self.s2_out, stream=stream)
+        hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
+                   miss_count, dgi=self.dgi, hot_size=self.hot_size,
+                   region_stride=self.region_stride, status=self.status, stream=stream)
+        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
+                  self.host_rows, status=self.status, stream=stream)
+        hs.sparse_decode(self.q_view(q), self.hot, self.hot, self.row_width, 0, self.hot.shape[0],
+                         hot_idx.view(R, 1, self.cap), count.view(R, 1), self.scale, self.d_v,
+                         out=self.out, lse=self.lse, workspace=self.workspace,
+                         status=self.status, stream=stream)
+        return self.out, self.lse
+
+    @staticmethod
+    def q_view(q):
+        return q if q.dtype == torch.bfloat16 else q.view(torch.bfloat16)
+
+    # Kernels of libhs launched by one step (index_copy_ above is torch's).
+    def launches_per_step(self):
+        ws = hs.sparse_decode_workspace_bytes(self.num_reqs, self.heads, 1, self.cap, self.d_qk,
+                                              self.d_v)
+        return 5 + (1 if ws > 0 else 0)

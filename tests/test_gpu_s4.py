@@ -1,0 +1,151 @@
+"""S4 parity: hs_sparse_decode (and the eq. (7) merge kernel) against the fp64
+oracle, within max |err| <= 1e-2 and relative L2 <= 5e-3 for bf16 inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import bits, check_attention, cuda
+from sparse_top_kv_gb300 import hs, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def decode_both(q, k, v, kv_rows, count, scale, d_v, row_stride, head_stride, sample_rows=None):
+    """q bf16 cuda [rows, H, d_qk]; k/v bf16 cuda caches (v may be k)."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = hs.sparse_decode(q, k, v, row_stride, head_stride, k.numel() // row_stride,
+                                cuda(kv_rows), None if count is None else cuda(count), scale,
+                                d_v, status=status)
+    torch.cuda.synchronize()
+    rows = np.arange(q.shape[0]) if sample_rows is None else np.asarray(sample_rows)
+    kb = bits(k).reshape(-1)
+    vb = kb if v.data_ptr() == k.data_ptr() else bits(v).reshape(-1)
+    ref_out, ref_lse = oracle.sparse_decode(bits(q)[rows], kb, vb, row_stride, head_stride,
+                                            kv_rows[rows],
+                                            None if count is None else count[rows], scale,
+                                            d_v=d_v)
+    check_attention(out[torch.from_numpy(rows).cuda()], lse[torch.from_numpy(rows).cuda()],
+                    ref_out, ref_lse)
+    return int(status.item())
+
+
+def random_sets(rng, rows, kv_heads, cap, n_kv, holes=True, empty_row=True):
+    kv_rows = np.full((rows, kv_heads, cap), -1, np.int32)
+    count = np.zeros((rows, kv_heads), np.int32)
+    for r in range(rows):
+        for g in range(kv_heads):
+            n = int(rng.integers(1, cap + 1))
+            if empty_row and r == rows - 1 and g == 0:
+                n = 0
+            kv_rows[r, g, :n] = rng.choice(n_kv, size=n, replace=False)
+            if holes and n > 4:
+                kv_rows[r, g, rng.integers(0, n, size=2)] = -1
+            count[r, g] = n
+    return kv_rows, count
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_gqa_small(group):
+    rng = np.random.default_rng(group)
+    rows, kv_heads, d, n_kv, cap = 3, 2, 128, 700, 300
+    heads = group * kv_heads
+    q = inputs.randn_bf16((rows, heads, d), 10 + group, device="cuda")
+    k = inputs.randn_bf16((n_kv, kv_heads, d), 20 + group, device="cuda")
+    v = inputs.randn_bf16((n_kv, kv_heads, d), 30 + group, device="cuda")
+    kv_rows, count = random_sets(rng, rows, kv_heads, cap, n_kv)
+    assert decode_both(q, k, v, kv_rows, count, 1 / math.sqrt(d), d, kv_heads * d, d) == 0
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_mla_small(heads):
+    rng = np.random.default_rng(heads)
+    rows, n_kv, cap = 3, 2000, 600
+    q = inputs.randn_bf16((rows, heads, 576), 40, device="cuda")
+    cache = inputs.randn_bf16((n_kv, 576), 41, device="cuda")
+    kv_rows, count = random_sets(rng, rows, 1, cap, n_kv)
+    assert decode_both(q, cache, cache, kv_rows, count, 1 / 24, 512, 576, 0) == 0
+
+
+def test_single_candidate_and_tail_sizes():
+    rng = np.random.default_rng(11)
+    n_kv = 400
+    cache = inputs.randn_bf16((n_kv, 576), 50, device="cuda")
+    for cap in (1, 15, 16, 17, 63, 64, 65, 129):
+        q = inputs.randn_bf16((2, 16, 576), 51 + cap, device="cuda")
+        kv_rows = np.stack([rng.choice(n_kv, size=cap, replace=False) for _ in range(2)])
+        decode_both(q, cache, cache, kv_rows[:, None].astype(np.int32), None, 1 / 24, 512, 576, 0)
+
+
+def test_out_of_range_rows_flagged_and_skipped():
+    cache = inputs.randn_bf16((100, 576), 60, device="cuda")
+    q = inputs.randn_bf16((1, 16, 576), 61, device="cuda")
+    kv_rows = np.array([[[3, 7, 100, 55, 1000]]], np.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = hs.sparse_decode(q, cache, cache, 576, 0, 100, cuda(kv_rows), None, 1 / 24, 512,
+                                status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 6
+    ref_out, ref_lse = oracle.sparse_decode(bits(q), bits(cache).reshape(-1),
+                                            bits(cache).reshape(-1), 576, 0,
+                                            np.array([[[3, 7, -1, 55, -1]]], np.int32), None,
+                                            1 / 24, d_v=512)
+    check_attention(out, lse, ref_out, ref_lse)
+
+
+def test_merge_states_kernel():
+    rng = np.random.default_rng(12)
+    n, parts, d = 37, 5, 512
+    m = rng.normal(size=(n, parts)) * 4
+    l = rng.uniform(0.5, 30, size=(n, parts))
+    o = rng.normal(size=(n, parts, d)) * l[..., None]
+    l[3, :] = 0  # an all-empty state
+    m[3, :] = -np.inf
+    l[5, 2] = 0  # one empty part
+    m[5, 2] = -np.inf
+    mt = torch.tensor(m, dtype=torch.float32, device="cuda")
+    lt = torch.tensor(l, dtype=torch.float32, device="cuda")
+    ot = torch.tensor(o, dtype=torch.float32, device="cuda")
+    out, lse = hs.merge_states(mt, lt, ot)
+    torch.cuda.synchronize()
+    # The kernel takes m in log2 units: convert for the natural-log oracle.
+    m32 = mt.double().cpu().numpy()
+    M, L, O = oracle.merge(m32 * math.log(2), lt.double().cpu().numpy(), ot.double().cpu().numpy())
+    ref = np.where(L[:, None] > 0, O / np.where(L > 0, L, 1)[:, None], 0.0)
+    ref_lse = np.where(L > 0, M + np.log(np.where(L > 0, L, 1)), -np.inf)
+    check_attention(out, lse, ref, ref_lse)
+
+
+def test_mla_decode_config_sampled():
+    """Full size (32 requests x 128 heads x 2048 rows from a 1.2 GB paged
+    cache), after S1; outputs of 3 sampled requests checked against the oracle."""
+    cfg = inputs.mla_decode()
+    R = cfg["num_reqs"]
+    tok, slot, count, err = hs.normalize_indices(
+        cuda(cfg["cand"]), torch.arange(R, dtype=torch.int32, device="cuda"),
+        torch.full((R,), cfg["ctx"], dtype=torch.int32, device="cuda"),
+        cuda(cfg["block_table"]), 64, num_pages=cfg["num_pages"])
+    kv_rows = slot.cpu().numpy()[:, None, :]
+    cnt = count.cpu().numpy()[:, None]
+    assert decode_both(cfg["q"], cfg["cache"], cfg["cache"], kv_rows, cnt, cfg["scale"], 512,
+                       576, 0, sample_rows=[0, 17, 31]) == 0
+
+
+def test_gqa_union_config_sampled():
+    """Full size (16 requests, 8 KV heads, 4.3 GB of bshd K/V), S1 union with
+    window and sinks then S4; 2 sampled requests checked against the oracle."""
+    cfg = inputs.gqa_union()
+    rows = cfg["cand"].shape[0]
+    R, G = cfg["num_reqs"], cfg["kv_heads"]
+    tok, slot, count, err = hs.normalize_indices(
+        cuda(cfg["cand"]), cuda(cfg["row_req"]),
+        torch.full((R,), cfg["ctx"], dtype=torch.int32, device="cuda"), cuda(cfg["block_table"]),
+        16, window=256, num_sinks=4, num_pages=cfg["num_pages"])
+    kv_rows = slot.cpu().numpy().reshape(R, G, -1)
+    cnt = count.cpu().numpy().reshape(R, G)
+    d = cfg["d"]
+    assert rows == R * G
+    assert decode_both(cfg["q"], cfg["k_cache"], cfg["v_cache"], kv_rows, cnt, cfg["scale"], d,
+                       G * d, d, sample_rows=[0, 15]) == 0
