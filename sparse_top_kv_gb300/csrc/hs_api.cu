@@ -41,4 +41,23 @@ int num_sms() {
     return n;
 }
 
+int ensure_dynamic_smem(const void* func, size_t bytes, int* cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && cache[dev] >= int(bytes)) return HS_OK;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) return HS_ERR_CUDA;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+        return HS_ERR_CUDA;
+    if (bytes + fa.sharedSizeBytes > size_t(optin)) return HS_ERR_CAPACITY;
+    if (bytes > 48 * 1024 &&
+        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) !=
+            cudaSuccess)
+        return HS_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cache[dev] = int(bytes);
+    return HS_OK;
+}
+
 }  // namespace hs_host

@@ -309,15 +309,10 @@ template <int DQK, int DV, int G, bool SHARED, int U>
 int launch(const AttnArgs& a, int units, hs_stream_t stream) {
     auto kern = attn_cc_kernel<DQK, DV, G, SHARED, U>;
     const size_t smem = size_t(kWarps) * G * (DV + 2) * sizeof(float);
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
-            return HS_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    static int smem_set[64] = {};
+    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem,
+                                                smem_set);
+    if (rc != HS_OK) return rc;
     dim3 grid(units, a.splits);
     kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();

@@ -173,6 +173,11 @@ namespace hs_host {
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// Opt `func` in to `bytes` of dynamic shared memory on the current device.
+// The attribute is raised only when a launch needs more than was set before
+// (per device); fails with HS_ERR_CAPACITY beyond the device's limit.
+int ensure_dynamic_smem(const void* func, size_t bytes, int* cache /* [64] */);
+
 inline int launch_status() {
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;

@@ -267,15 +267,10 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
     const size_t smem = size_t(8) * (size_t(1) << log2n) + size_t(4) * cap +
                         size_t(4) * hot_size;
     if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxSmem) != cudaSuccess)
-            return HS_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    static int smem_set[64] = {};
+    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(lookup_kernel),
+                                                smem, smem_set);
+    if (rc != HS_OK) return rc;
     LookupArgs a{slot,     count,    rows,     cap,        num_real_rows, newest_slot,
                  dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
                  miss_src, miss_dst, miss_count, stats,    err,           log2n};

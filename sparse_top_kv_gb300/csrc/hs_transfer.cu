@@ -275,15 +275,10 @@ constexpr int kMaxSmem = 227 * 1024;
 int launch_xfer(const XferArgs& a, int64_t max_items, hs_stream_t stream) {
     const size_t smem = xfer_smem_bytes(a.nlists);
     if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(xfer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxSmem) != cudaSuccess)
-            return HS_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    static int smem_set[64] = {};
+    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(xfer_kernel), smem,
+                                                smem_set);
+    if (rc != HS_OK) return rc;
     const int64_t grid = hs::max64(1, hs::min64(max_items, hs_host::num_sms()));
     xfer_kernel<<<int(grid), kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();

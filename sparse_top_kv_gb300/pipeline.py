@@ -70,29 +70,38 @@ class HiSparseDecoder:
             num_pages=self.num_pages)
         return slot.view(-1).clone()
 
-    def step(self, cand, seq_lens, newest_slot, new_row, q, stream=None):
+    def step(self, cand, seq_lens, newest_slot, new_row, q, stream=None, events=None):
         """cand int32 [R, top_k] positions; seq_lens int32 [R]; newest_slot int32
         [R]; new_row [R, row_width] (the new token's KV row); q bf16 [R, H, d_qk].
-        Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated."""
+        Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated.
+        `events`, if given, is a list of 6 CUDA events recorded before S1 and
+        after S1, S2, SwapIn, BackUp and S4."""
         R = self.num_reqs
+        rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         # The model's KV write of the newest token (stand-in): reserved hot rows.
         self.hot.index_copy_(0, self.reserved_rows, new_row)
+        rec(0)
         tok, slot, count, err = hs.normalize_indices(
             cand, self.row_req, seq_lens, self.block_table, self.page_size,
             window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
             out=self.s1_out, stream=stream)
+        rec(1)
         hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr = hs.hot_lookup_assign(
             slot, count, newest_slot, self.dgi, self.lru, self.region_stride, self.stats,
             out=self.s2_out, stream=stream)
+        rec(2)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
                    region_stride=self.region_stride, status=self.status, stream=stream)
+        rec(3)
         hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
                   self.host_rows, status=self.status, stream=stream)
+        rec(4)
         hs.sparse_decode(self.q_view(q), self.hot, self.hot, self.row_width, 0, self.hot.shape[0],
                          hot_idx.view(R, 1, self.cap), count.view(R, 1), self.scale, self.d_v,
                          out=self.out, lse=self.lse, workspace=self.workspace,
                          status=self.status, stream=stream)
+        rec(5)
         return self.out, self.lse
 
     @staticmethod
