@@ -46,7 +46,7 @@ class OracleHiSparse:
         swap_in(self.pool, self.hot.reshape(-1), self.row_bytes, msrc, mdst, mcount,
                 dgi=self.dgi, hot_size=hs_, region_stride=rs)
         bad = backup(self.hot.reshape(-1), reserved, self.pool, newest_slot, self.row_bytes)
-        rows = np.arange(R) if attend_rows is None else np.asarray(attend_rows)
+        rows = np.arange(R) if attend_rows is None else np.asarray(attend_rows, dtype=np.int64)
         hot_bf16 = self.hot.view(np.uint16).reshape(-1)
         width = self.row_bytes // 2
         out, lse = sparse_decode(q_bits[rows], hot_bf16, hot_bf16, width, 0,
