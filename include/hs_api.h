@@ -217,6 +217,38 @@ int hs_sparse_decode(const void* q, const void* k_base, const void* v_base, int6
                      int64_t workspace_bytes, int32_t* status, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * hs_sparse_decode_noalloc -- the paper has no counterpart; this is a
+ * convenience of this library.
+ *
+ * Same arguments and results as hs_sparse_decode, minus the workspace: the
+ * split-KV partial states go to a scratch array compiled into libhs
+ * (HS_NOALLOC_WORKSPACE_BYTES per GPU, held by every GPU that loads the
+ * library until the process exits).  It is meant for callers that must not
+ * allocate device memory on the decode path -- plugin code running inside a
+ * host engine that owns every device allocation, or latency-critical loops
+ * where a cudaMalloc (which may synchronise the device) is not allowed.
+ * No allocation happens in this call.
+ *
+ * - Shapes whose workspace (hs_sparse_decode_workspace_bytes) exceeds
+ *   HS_NOALLOC_WORKSPACE_BYTES are rejected with HS_ERR_CAPACITY.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Every call on a device shares the one array, which keeps the previous
+ *   call's contents (nothing in it needs to start at zero).  Calls whose
+ *   executions overlap on the GPU (e.g. on two streams) race on it: order
+ *   them on one stream or use hs_sparse_decode with separate workspaces.
+ * ------------------------------------------------------------------------- */
+#define HS_NOALLOC_WORKSPACE_BYTES (8 * 1024 * 1024)
+
+int hs_sparse_decode_noalloc(const void* q, const void* k_base, const void* v_base,
+                             int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
+                             const int32_t* kv_rows, const int32_t* count, int32_t rows,
+                             int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
+                             int32_t d_v, float scale, void* out, float* lse, int32_t* status,
+                             hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * hs_merge_states -- [PT] 3.2 eq. (7) / [PA] 1.4 combine, the split-KV merge
  * used inside hs_sparse_decode, exposed for testing.
  * m, l       fp32 [n, parts]: per-part maximum logit in log2 units (logit *

@@ -407,3 +407,45 @@ extern "C" int hs_merge_states(const float* m, const float* l, const float* o, i
         m, l, o, parts, d_v, static_cast<__nv_bfloat16*>(out), lse);
     return hs_host::launch_status();
 }
+
+// ----------------------------------------------------------------------------
+// Allocation-free variant of hs_sparse_decode: the split-KV partial states
+// live in a scratch array compiled into the library, for callers that may
+// not allocate device memory on the decode path.  The array's device address
+// is looked up once per device (cudaGetSymbolAddress, with that device
+// current) on the first call there; the host-side name of the array is only
+// a stand-in and is never passed to a kernel.
+namespace {
+__device__ __align__(256) unsigned char g_noalloc_workspace[HS_NOALLOC_WORKSPACE_BYTES];
+void* g_noalloc_workspace_dev[64] = {};
+}  // namespace
+
+extern "C" int hs_sparse_decode_noalloc(const void* q, const void* k_base, const void* v_base,
+                                        int64_t row_stride, int64_t kv_head_stride,
+                                        int64_t num_kv_rows, const int32_t* kv_rows,
+                                        const int32_t* count, int32_t rows, int32_t cap,
+                                        int32_t heads, int32_t kv_heads, int32_t d_qk,
+                                        int32_t d_v, float scale, void* out, float* lse,
+                                        int32_t* status, hs_stream_t stream) {
+    const int64_t need =
+        hs_sparse_decode_workspace_bytes(rows, heads, kv_heads, cap, d_qk, d_v);
+    if (need > int64_t(HS_NOALLOC_WORKSPACE_BYTES)) return HS_ERR_CAPACITY;
+    void* ws = nullptr;
+    if (need > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+        if (dev < 0 || dev >= 64) return HS_ERR_UNSUPPORTED;
+        if (g_noalloc_workspace_dev[dev] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr) {
+                cudaGetLastError();
+                return HS_ERR_CUDA;
+            }
+            g_noalloc_workspace_dev[dev] = p;
+        }
+        ws = g_noalloc_workspace_dev[dev];
+    }
+    return hs_sparse_decode(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows,
+                            count, rows, cap, heads, kv_heads, d_qk, d_v, scale, out, lse, ws,
+                            need, status, stream);
+}

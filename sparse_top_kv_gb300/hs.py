@@ -45,7 +45,11 @@ _SIGS = {
     "hs_sparse_decode": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32,
                           _I32, _F32, _P, _P, _P, _I64, _P, _P], ctypes.c_int),
     "hs_merge_states": ([_P, _P, _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "hs_sparse_decode_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
+                                  _I32, _I32, _F32, _P, _P, _P, _P], ctypes.c_int),
 }
+
+NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024  # HS_NOALLOC_WORKSPACE_BYTES
 
 EXPORTS = tuple(_SIGS)
 
@@ -234,4 +238,24 @@ def merge_states(m, l, o, *, out=None, lse=None, stream=None):
         lse = torch.empty(n, dtype=torch.float32, device=o.device)
     _call("hs_merge_states", _ptr(m), _ptr(l), _ptr(o), n, parts, d_v, _ptr(out), _ptr(lse),
           _stream(stream))
+    return out, lse
+
+
+def sparse_decode_noalloc(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows,
+                          count, scale, d_v, *, out, lse, status=None, stream=None):
+    """S4 without a workspace argument: for callers that may not allocate
+    device memory on the decode path (the library's built-in scratch array is
+    used; see hs_sparse_decode_noalloc in hs_api.h).  `out` and `lse` must be
+    passed in, so that this call allocates nothing."""
+    _check(q, torch.bfloat16, "q")
+    _check(kv_rows, torch.int32, "kv_rows")
+    _check(count, torch.int32, "count")
+    _check(out, torch.bfloat16, "out")
+    _check(lse, torch.float32, "lse")
+    _check(status, torch.int32, "status")
+    rows, heads, d_qk = q.shape
+    _, kv_heads, cap = kv_rows.shape
+    _call("hs_sparse_decode_noalloc", _ptr(q), _ptr(k_base), _ptr(v_base), row_stride,
+          kv_head_stride, num_kv_rows, _ptr(kv_rows), _ptr(count), rows, cap, heads, kv_heads,
+          d_qk, d_v, float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
     return out, lse
