@@ -23,6 +23,7 @@
 
 #include <algorithm>
 
+#include "hs_attention_internal.cuh"
 #include "hs_common.cuh"
 
 namespace hs_attn {
@@ -270,7 +271,7 @@ __global__ void merge_kernel(const float* __restrict__ pm, const float* __restri
 // Host side: kernel choice and split policy.
 
 struct Plan {
-    int kind;  // 0 unsupported, 1 MLA (576/512 shared row), 2 GQA d=128
+    int kind;  // 0 unsupported, 1 MLA on CUDA cores, 2 GQA d=128, 3 MLA on tcgen05
     int G;     // heads per CTA
     int chunks_per_kvh;
     int splits;
@@ -280,7 +281,21 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     Plan p{0, 0, 0, 1};
     if (rows <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads) return p;
     const int group = heads / kv_heads;
-    if (d_qk == 576 && d_v == 512 && kv_heads == 1 && shared && heads % 4 == 0) {
+    const bool mla = d_qk == 576 && d_v == 512 && kv_heads == 1 && shared;
+    if (mla && mla_tc_head_group(heads) > 0) {
+        // Tensor-core kernel: one CTA per SM (about 220 KB of shared memory);
+        // split the candidate list so that the grid fills the SMs once.
+        p.kind = 3;
+        p.G = mla_tc_head_group(heads);
+        p.chunks_per_kvh = heads / p.G;
+        const int64_t units = int64_t(rows) * p.chunks_per_kvh;
+        const int64_t sms = hs_host::num_sms();
+        int64_t s = units >= sms ? 1 : sms / units;
+        s = hs::min64(s, hs::max64(1, (cap + 127) / 128));
+        p.splits = int(hs::max64(1, hs::min64(s, 64)));
+        return p;
+    }
+    if (mla && heads % 4 == 0) {
         p.kind = 1;
         p.G = 4;
     } else if (d_qk == 128 && d_v == 128 && (group == 1 || group == 2 || group == 4 || group == 8)) {
@@ -381,7 +396,28 @@ extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v
     }
     const int units = rows * kv_heads * p.chunks_per_kvh;
     int rc;
-    if (p.kind == 1) {
+    if (p.kind == 3) {
+        MlaArgs m{};
+        m.q = a.q;
+        m.kv = a.k;
+        m.row_stride = row_stride;
+        m.num_kv_rows = num_kv_rows;
+        m.kv_rows = kv_rows;
+        m.count = count;
+        m.rows = rows;
+        m.cap = cap;
+        m.heads = heads;
+        m.scale_log2 = a.scale_log2;
+        m.out = a.out;
+        m.lse = lse;
+        m.part_m = a.part_m;
+        m.part_l = a.part_l;
+        m.part_o = a.part_o;
+        m.splits = p.splits;
+        m.status = status;
+        m.timeout_ns = hs::kWaitTimeoutNs;
+        rc = launch_mla_tc(m, p.G, dim3(units, p.splits), stream);
+    } else if (p.kind == 1) {
         rc = launch<576, 512, 4, true, 2>(a, units, stream);
     } else {
         switch (p.G) {

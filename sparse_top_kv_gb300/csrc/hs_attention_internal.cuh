@@ -1,0 +1,35 @@
+// hs_attention_internal.cuh -- internal interface between the S4 dispatcher
+// (hs_attention.cu) and the tensor-core MLA kernel (hs_attention_mla.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "hs_common.cuh"
+
+namespace hs_attn {
+
+struct MlaArgs {
+    const __nv_bfloat16* q;   // [rows, heads, 576]
+    const __nv_bfloat16* kv;  // rows of row_stride elements; K = [0,576), V = [0,512)
+    int64_t row_stride;
+    int64_t num_kv_rows;
+    const int32_t* kv_rows;   // [rows, cap]
+    const int32_t* count;     // [rows] or nullptr
+    int32_t rows, cap, heads;
+    float scale_log2;
+    __nv_bfloat16* out;       // [rows, heads, 512]
+    float* lse;               // [rows, heads] or nullptr
+    float* part_m;            // split partial states (splits > 1)
+    float* part_l;
+    float* part_o;
+    int32_t splits;
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+// Query heads handled by one CTA (64, 32 or 16), or 0 when heads % 16 != 0.
+int mla_tc_head_group(int heads);
+// grid = (rows * heads / hg, splits).
+int launch_mla_tc(const MlaArgs& a, int hg, dim3 grid, hs_stream_t stream);
+
+}  // namespace hs_attn

@@ -69,6 +69,19 @@ def test_mla_small(heads):
     assert decode_both(q, cache, cache, kv_rows, count, 1 / 24, 512, 576, 0) == 0
 
 
+@pytest.mark.parametrize("rows,heads,cap", [(152, 16, 384), (76, 128, 256), (200, 32, 300)])
+def test_mla_many_tiles_per_cta(rows, heads, cap):
+    """Enough rows that each CTA walks several 128-row tiles of its list."""
+    rng = np.random.default_rng(rows + heads)
+    n_kv = 20000
+    q = inputs.randn_bf16((rows, heads, 576), 42, device="cuda")
+    cache = inputs.randn_bf16((n_kv, 576), 43, device="cuda")
+    kv_rows, count = random_sets(rng, rows, 1, cap, n_kv)
+    count[:, 0] = np.maximum(count[:, 0], cap - 5)
+    assert decode_both(q, cache, cache, kv_rows, count, 1 / 24, 512, 576, 0,
+                       sample_rows=[0, 1, rows // 2, rows - 1]) == 0
+
+
 def test_single_candidate_and_tail_sizes():
     rng = np.random.default_rng(11)
     n_kv = 400
