@@ -48,16 +48,38 @@ def randn_bf16(shape, seed, device="cpu"):
     return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
+def pinned_empty(shape, dtype):
+    """Pinned host tensor whose pages are first touched by the CPU."""
+    out = torch.empty(*shape, dtype=dtype, pin_memory=True)
+    flat = out.view(-1).view(torch.uint8)
+    flat[::4096].zero_()
+    return out
+
+
+def host_read_pass(t):
+    """Read every 64-byte line of a host tensor on the CPU.
+
+    Measured on GB300 (Grace host, NVLink-C2C): host lines last written by
+    the GPU (D2H copies) are read back by GPU kernels 10-40x slower than
+    lines the CPU has read since (first GPU read of a row 2-6 ms for 19K
+    rows instead of 0.15 ms).  A pool that the GPU filled is passed over
+    once by the CPU before use."""
+    flat = t.view(-1).view(torch.uint8)
+    n = flat.numel() // 64 * 64
+    return int(flat[:n].view(-1, 64)[:, 0].sum())
+
+
 def fill_randn_bf16_pinned(rows, width, seed, chunk_rows=1 << 20):
     """A pinned host tensor [rows, width] bf16 of N(0,1) values, generated on the
     GPU in chunks (seeded) and copied down; used for the multi-GB host pools."""
-    out = torch.empty(rows, width, dtype=torch.bfloat16, pin_memory=True)
+    out = pinned_empty((rows, width), torch.bfloat16)
     g = torch.Generator(device="cuda").manual_seed(seed)
     for r0 in range(0, rows, chunk_rows):
         r1 = min(rows, r0 + chunk_rows)
         blk = torch.randn(r1 - r0, width, generator=g, device="cuda").to(torch.bfloat16)
         out[r0:r1].copy_(blk)
     torch.cuda.synchronize()
+    host_read_pass(out)
     return out
 
 
@@ -163,7 +185,7 @@ def swapin(num_reqs=64, misses=4096, pool_rows=1 << 20, row_bytes=1152, seed=Non
     miss source ids (sorted), and BackUp destinations."""
     seed = SEEDS["swapin"] if seed is None else seed
     rng = _rng(seed)
-    pool = torch.empty(pool_rows, row_bytes, dtype=torch.uint8, pin_memory=True)
+    pool = pinned_empty((pool_rows, row_bytes), torch.uint8)
     g = torch.Generator(device="cuda").manual_seed(seed)
     chunk = 1 << 18
     for r0 in range(0, pool_rows, chunk):
@@ -171,6 +193,7 @@ def swapin(num_reqs=64, misses=4096, pool_rows=1 << 20, row_bytes=1152, seed=Non
         pool[r0:r1].copy_(torch.randint(0, 256, (r1 - r0, row_bytes), generator=g,
                                         device="cuda", dtype=torch.uint8))
     torch.cuda.synchronize()
+    host_read_pass(pool)
     src = np.empty((num_reqs, misses), np.int32)
     half = num_reqs // 2
     run = 64
