@@ -130,6 +130,10 @@ int hs_hot_state_reset(int32_t* dgi, int16_t* lru, int32_t rows, int32_t hot_siz
  * stats       int64 [2]: {hits, misses} accumulated (atomically added).
  * err         int32 [rows]: entries dropped as repeats of an earlier entry
  *             of the row (only the first occurrence resolves).
+ * hit_idx     int32 [rows, cap] or NULL: hot_idx with the misses set to -1
+ *             (the rows that are already resident before the SwapIn).
+ * miss_rows   int32 [rows, cap] or NULL: int32 copy of miss_dst (first
+ *             miss_count[r] entries valid, the rest -1).
  * Semantics (bit-exact): walk lru from least to most recently used; a slot
  * whose dgi is among the row's pending ids is a hit; the rest, in LRU order,
  * are the evictable list E.  Misses, in row order m = 0, 1, .., take E[m].
@@ -140,7 +144,7 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
                          int16_t* lru, int32_t hot_size, int64_t region_stride,
                          int32_t* hot_idx, uint8_t* miss_mask, int32_t* miss_src,
                          int64_t* miss_dst, int32_t* miss_count, int64_t* stats, int32_t* err,
-                         hs_stream_t stream);
+                         int32_t* hit_idx, int32_t* miss_rows, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * S3  hs_swap_in -- [HS] Phase 5 (copy each miss row host -> hot; a source
@@ -215,6 +219,33 @@ int hs_sparse_decode(const void* q, const void* k_base, const void* v_base, int6
                      int32_t rows, int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
                      int32_t d_v, float scale, void* out, float* lse, void* workspace,
                      int64_t workspace_bytes, int32_t* status, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hs_sparse_decode_partial -- S4 over a subset of a row's candidates, left as
+ * unnormalised partial states to be combined with others by eq. (7)
+ * (hs_merge_states).  [PT] 3.2 eq. (7): o_s must stay unnormalised until the
+ * merge.  Used to attend over the rows already resident while the SwapIn of
+ * the missing rows is still in flight, then over the swapped rows, and merge.
+ *
+ * Same inputs as hs_sparse_decode (no out / lse / workspace).  Writes, for
+ * every (row, head) qh, the columns [part_base, part_base + P) of
+ *   part_m fp32 [rows*heads, parts_total]      max logit, log2 units (-inf: empty)
+ *   part_l fp32 [rows*heads, parts_total]      sum of 2^(s - m)      (0: empty)
+ *   part_o fp32 [rows*heads, parts_total, d_v] sum of 2^(s - m) V
+ * where P = hs_sparse_decode_partial_splits(rows, heads, kv_heads, cap,
+ * d_qk, d_v) (every one of the P columns is written, empty ones with l = 0).
+ * part_base + P > parts_total is HS_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+int32_t hs_sparse_decode_partial_splits(int32_t rows, int32_t heads, int32_t kv_heads,
+                                        int32_t cap, int32_t d_qk, int32_t d_v);
+
+int hs_sparse_decode_partial(const void* q, const void* k_base, const void* v_base,
+                             int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
+                             const int32_t* kv_rows, const int32_t* count, int32_t rows,
+                             int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
+                             int32_t d_v, float scale, float* part_m, float* part_l,
+                             float* part_o, int32_t parts_total, int32_t part_base,
+                             int32_t* status, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hs_sparse_decode_noalloc -- the paper has no counterpart; this is a

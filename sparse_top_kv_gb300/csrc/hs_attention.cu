@@ -46,9 +46,10 @@ struct AttnArgs {
     float* lse;
     float* part_m;  // [rows*heads, splits]
     float* part_l;
-    float* part_o;  // [rows*heads, splits, d_v]
+    float* part_o;  // [rows*heads, part_stride, d_v]
     int32_t splits, chunks_per_kvh;
     int32_t* status;
+    int32_t part_stride, part_base, force_partial;
 };
 
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
@@ -227,15 +228,16 @@ __global__ void __launch_bounds__(kThreads) attn_cc_kernel(const AttnArgs a) {
             }
         }
         const int64_t qh = int64_t(row) * a.heads + h0 + h;
-        if (a.splits == 1) {
+        if (a.splits == 1 && !a.force_partial) {
             a.out[qh * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
             if (d == 0 && a.lse != nullptr)
                 a.lse[qh] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
         } else {
-            a.part_o[(qh * a.splits + split) * DV + d] = O;
+            const int64_t pi = qh * a.part_stride + a.part_base + split;
+            a.part_o[pi * DV + d] = O;
             if (d == 0) {
-                a.part_m[qh * a.splits + split] = M;
-                a.part_l[qh * a.splits + split] = L;
+                a.part_m[pi] = M;
+                a.part_l[pi] = L;
             }
         }
     }
@@ -344,29 +346,61 @@ extern "C" int64_t hs_sparse_decode_workspace_bytes(int32_t rows, int32_t heads,
     return workspace_bytes(p, rows, heads, d_v);
 }
 
-extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v_base,
-                                int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
-                                const int32_t* kv_rows, const int32_t* count, int32_t rows,
-                                int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
-                                int32_t d_v, float scale, void* out, float* lse,
-                                void* workspace, int64_t workspace_bytes_given, int32_t* status,
-                                hs_stream_t stream) {
+namespace {
+
+struct PartialOut {
+    float* m;
+    float* l;
+    float* o;
+    int32_t parts_total;
+    int32_t part_base;
+};
+
+int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t row_stride,
+                int64_t kv_head_stride, int64_t num_kv_rows, const int32_t* kv_rows,
+                const int32_t* count, int32_t rows, int32_t cap, int32_t heads, int32_t kv_heads,
+                int32_t d_qk, int32_t d_v, float scale, void* out, float* lse, void* workspace,
+                int64_t workspace_bytes_given, const PartialOut* po, int32_t* status,
+                hs_stream_t stream) {
     if (rows < 0 || cap < 0 || heads <= 0 || kv_heads <= 0 || d_qk <= 0 || d_v <= 0 ||
         row_stride <= 0 || kv_head_stride < 0 || num_kv_rows < 0)
         return HS_ERR_INVALID_ARG;
     if (rows == 0) return HS_OK;
-    if (q == nullptr || k_base == nullptr || v_base == nullptr || out == nullptr ||
-        (cap > 0 && kv_rows == nullptr))
+    if (q == nullptr || k_base == nullptr || v_base == nullptr ||
+        (po == nullptr && out == nullptr) || (cap > 0 && kv_rows == nullptr))
         return HS_ERR_INVALID_ARG;
     const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!al(q) || !al(k_base) || !al(v_base) || !al(out) || row_stride % 8 || kv_head_stride % 8)
+    if (!al(q) || !al(k_base) || !al(v_base) || (out != nullptr && !al(out)) ||
+        row_stride % 8 || kv_head_stride % 8)
         return HS_ERR_MISALIGNED;
     const bool shared = k_base == v_base;
     const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, shared);
     if (p.kind == 0) return HS_ERR_UNSUPPORTED;
-    const int64_t ws = workspace_bytes(p, rows, heads, d_v);
-    if (ws > 0 && (workspace == nullptr || workspace_bytes_given < ws)) return HS_ERR_CAPACITY;
+    const int64_t n = int64_t(rows) * heads;
     AttnArgs a{};
+    if (po != nullptr) {
+        if (po->m == nullptr || po->l == nullptr || po->o == nullptr || po->part_base < 0 ||
+            po->part_base + p.splits > po->parts_total)
+            return HS_ERR_INVALID_ARG;
+        a.part_m = po->m;
+        a.part_l = po->l;
+        a.part_o = po->o;
+        a.part_stride = po->parts_total;
+        a.part_base = po->part_base;
+        a.force_partial = 1;
+    } else {
+        const int64_t ws = workspace_bytes(p, rows, heads, d_v);
+        if (ws > 0 && (workspace == nullptr || workspace_bytes_given < ws)) return HS_ERR_CAPACITY;
+        if (p.splits > 1) {
+            float* w = static_cast<float*>(workspace);
+            a.part_m = w;
+            a.part_l = w + n * p.splits;
+            a.part_o = w + 2 * n * p.splits;
+        }
+        a.part_stride = p.splits;
+        a.part_base = 0;
+        a.force_partial = 0;
+    }
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.k = static_cast<const __nv_bfloat16*>(k_base);
     a.v = static_cast<const __nv_bfloat16*>(v_base);
@@ -387,13 +421,6 @@ extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v
     a.splits = p.splits;
     a.chunks_per_kvh = p.chunks_per_kvh;
     a.status = status;
-    const int64_t n = int64_t(rows) * heads;
-    if (p.splits > 1) {
-        float* w = static_cast<float*>(workspace);
-        a.part_m = w;
-        a.part_l = w + n * p.splits;
-        a.part_o = w + 2 * n * p.splits;
-    }
     const int units = rows * kv_heads * p.chunks_per_kvh;
     int rc;
     if (p.kind == 3) {
@@ -414,6 +441,9 @@ extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v
         m.part_l = a.part_l;
         m.part_o = a.part_o;
         m.splits = p.splits;
+        m.part_stride = a.part_stride;
+        m.part_base = a.part_base;
+        m.force_partial = a.force_partial;
         m.status = status;
         m.timeout_ns = hs::kWaitTimeoutNs;
         rc = launch_mla_tc(m, p.G, dim3(units, p.splits), stream);
@@ -427,10 +457,44 @@ extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v
             default: rc = launch<128, 128, 8, false, 2>(a, units, stream); break;
         }
     }
-    if (rc != HS_OK || p.splits == 1) return rc;
+    if (rc != HS_OK || po != nullptr || p.splits == 1) return rc;
     merge_kernel<<<int(n), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         a.part_m, a.part_l, a.part_o, p.splits, d_v, a.out, lse);
     return hs_host::launch_status();
+}
+
+}  // namespace
+
+extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v_base,
+                                int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
+                                const int32_t* kv_rows, const int32_t* count, int32_t rows,
+                                int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
+                                int32_t d_v, float scale, void* out, float* lse,
+                                void* workspace, int64_t workspace_bytes_given, int32_t* status,
+                                hs_stream_t stream) {
+    return decode_impl(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
+                       rows, cap, heads, kv_heads, d_qk, d_v, scale, out, lse, workspace,
+                       workspace_bytes_given, nullptr, status, stream);
+}
+
+extern "C" int32_t hs_sparse_decode_partial_splits(int32_t rows, int32_t heads, int32_t kv_heads,
+                                                   int32_t cap, int32_t d_qk, int32_t d_v) {
+    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, kv_heads == 1 && d_qk == 576);
+    return p.kind == 0 ? 0 : p.splits;
+}
+
+extern "C" int hs_sparse_decode_partial(const void* q, const void* k_base, const void* v_base,
+                                        int64_t row_stride, int64_t kv_head_stride,
+                                        int64_t num_kv_rows, const int32_t* kv_rows,
+                                        const int32_t* count, int32_t rows, int32_t cap,
+                                        int32_t heads, int32_t kv_heads, int32_t d_qk,
+                                        int32_t d_v, float scale, float* part_m, float* part_l,
+                                        float* part_o, int32_t parts_total, int32_t part_base,
+                                        int32_t* status, hs_stream_t stream) {
+    const PartialOut po{part_m, part_l, part_o, parts_total, part_base};
+    return decode_impl(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
+                       rows, cap, heads, kv_heads, d_qk, d_v, scale, nullptr, nullptr, nullptr, 0,
+                       &po, status, stream);
 }
 
 extern "C" int hs_merge_states(const float* m, const float* l, const float* o, int32_t n,

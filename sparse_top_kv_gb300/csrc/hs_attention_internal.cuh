@@ -19,10 +19,13 @@ struct MlaArgs {
     float scale_log2;
     __nv_bfloat16* out;       // [rows, heads, 512]
     float* lse;               // [rows, heads] or nullptr
-    float* part_m;            // split partial states (splits > 1)
+    float* part_m;            // partial states, index (row*heads+h)*part_stride + part_base + split
     float* part_l;
     float* part_o;
     int32_t splits;
+    int32_t part_stride;
+    int32_t part_base;
+    int32_t force_partial;    // 1: write partial states even when splits == 1
     int32_t* status;
     uint64_t timeout_ns;
 };

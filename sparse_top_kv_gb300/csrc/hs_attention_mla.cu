@@ -483,11 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
 #pragma unroll
                         for (int h = 0; h < HG; ++h) {
                             const int64_t qh = qh0 + h;
-                            if (a.splits == 1) {
+                            if (a.splits == 1 && !a.force_partial) {
                                 a.out[qh * 512 + d] =
                                     __float2bfloat16_rn(L[h] > 0.f ? o[h] / L[h] : 0.f);
                             } else {
-                                a.part_o[(qh * a.splits + split) * 512 + d] = L[h] > 0.f ? o[h] : 0.f;
+                                a.part_o[(qh * a.part_stride + a.part_base + split) * 512 + d] =
+                                    L[h] > 0.f ? o[h] : 0.f;
                             }
                         }
                     }
@@ -497,13 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                         for (int h = 0; h < HG; ++h)
                             if (h == tid) { Lh = L[h]; Mh = m_ref[h]; }
                         const int64_t qh = qh0 + tid;
-                        if (a.splits == 1) {
+                        if (a.splits == 1 && !a.force_partial) {
                             if (a.lse)
                                 a.lse[qh] = Lh > 0.f ? (Mh + log2f(Lh)) * 0.6931471805599453f
                                                      : -CUDART_INF_F;
                         } else {
-                            a.part_m[qh * a.splits + split] = Lh > 0.f ? Mh : -CUDART_INF_F;
-                            a.part_l[qh * a.splits + split] = Lh;
+                            const int64_t pi = qh * a.part_stride + a.part_base + split;
+                            a.part_m[pi] = Lh > 0.f ? Mh : -CUDART_INF_F;
+                            a.part_l[pi] = Lh;
                         }
                     }
                 }

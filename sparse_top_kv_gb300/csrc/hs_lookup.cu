@@ -8,10 +8,11 @@
 // open-addressing hash of the row's pending slot ids in shared memory; the
 // first occurrence of a repeated id is kept with atomicMin on its position,
 // so repeats resolve deterministically (the walkthrough's hash overwrites on
-// a repeated key, which is racy).  Phase 2 walks the LRU list in 1024-wide
-// chunks; hits and evictables are compacted in LRU order by a block-wide
-// ballot/popc/shuffle scan.  Phase 3 ranks the misses in row order with the
-// same scan and hands them E[0], E[1], ...  Phase 4 writes
+// a repeated key, which is racy).  Phase 2 walks the LRU list with each
+// thread owning a contiguous run of positions (dgi and lru staged in shared
+// memory); hits and evictables are compacted in LRU order by one block-wide
+// shuffle scan.  Phase 3 ranks the misses in row order with the same scan and
+// hands them E[0], E[1], ...  Phase 4 writes
 // E[M:] ++ E[:M] ++ hits.  The output is bit-identical to the sequential
 // definition for every thread schedule.
 #include "hs_common.cuh"
@@ -40,6 +41,8 @@ struct LookupArgs {
     int64_t* stats;
     int32_t* err;
     int32_t hash_log2;
+    int32_t* hit_idx;    // optional: hot_idx with the misses set to -1
+    int32_t* miss_rows;  // optional: int32 copy of miss_dst
 };
 
 __device__ __forceinline__ uint32_t hash_of(int32_t g, int log2n) {
@@ -65,21 +68,25 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     __shared__ int s_dup;
 
     const int HS = 1 << a.hash_log2;
+    const int cap = a.cap;
+    const int hot_size = a.hot_size;
     int32_t* keys = reinterpret_cast<int32_t*>(smem);
     int32_t* vals = keys + HS;
     int32_t* state = vals + HS;
-    int16_t* E = reinterpret_cast<int16_t*>(state + a.cap);
-    int16_t* H = E + a.hot_size;
+    int32_t* s_dgi = state + cap;
+    int16_t* s_lru = reinterpret_cast<int16_t*>(s_dgi + hot_size);
+    int16_t* E = s_lru + hot_size;
+    int16_t* H = E + hot_size;
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
-    const int cap = a.cap;
-    const int hot_size = a.hot_size;
     const int32_t* g_row = a.slot + int64_t(row) * cap;
     int32_t* out = a.hot_idx + int64_t(row) * cap;
     uint8_t* mm = a.miss_mask ? a.miss_mask + int64_t(row) * cap : nullptr;
     int32_t* msrc = a.miss_src + int64_t(row) * cap;
     int64_t* mdst = a.miss_dst + int64_t(row) * cap;
+    int32_t* hidx = a.hit_idx ? a.hit_idx + int64_t(row) * cap : nullptr;
+    int32_t* mrow = a.miss_rows ? a.miss_rows + int64_t(row) * cap : nullptr;
 
     if (row >= a.num_real_rows) {  // CUDA-graph padding row
         for (int i = tid; i < cap; i += kThreads) {
@@ -87,6 +94,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
             if (mm) mm[i] = 0;
             msrc[i] = -1;
             mdst[i] = -1;
+            if (hidx) hidx[i] = -1;
+            if (mrow) mrow[i] = -1;
         }
         if (tid == 0) {
             a.miss_count[row] = 0;
@@ -98,6 +107,11 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     int16_t* lru = a.lru + int64_t(row) * hot_size;
     const int64_t hot_base = int64_t(row) * a.region_stride;
 
+    // Stage the row's state (coalesced) and clear the hash.
+    for (int j = tid; j < hot_size; j += kThreads) {
+        s_dgi[j] = dgi[j];
+        s_lru[j] = lru[j];
+    }
     for (int h = tid; h < HS; h += kThreads) {
         keys[h] = kEmpty;
         vals[h] = INT32_MAX;
@@ -115,11 +129,14 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         if (mm) mm[i] = 0;
         msrc[i] = -1;
         mdst[i] = -1;
+        if (mrow) mrow[i] = -1;
         if (g < 0) {
             out[i] = -1;
+            if (hidx) hidx[i] = -1;
             state[i] = kDone;
         } else if (newest >= 0 && g == newest) {
             out[i] = int32_t(hot_base + hot_size);
+            if (hidx) hidx[i] = int32_t(hot_base + hot_size);
             state[i] = kDone;
         } else {
             uint32_t h = hash_of(g, a.hash_log2);
@@ -145,6 +162,7 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
             if (h >= 0 && vals[h] != i) {
                 state[i] = kDone;
                 out[i] = -1;
+                if (hidx) hidx[i] = -1;
                 ++dups;
             }
         }
@@ -152,69 +170,83 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     }
     __syncthreads();
 
-    // Phase 2: LRU walk, least -> most recently used.
-    int hits_total = 0;
-    for (int base = 0; base < hot_size; base += kThreads) {
-        const int pos = base + tid;
-        int hit = 0;
-        int16_t s = -1;
-        if (pos < hot_size) {
-            s = lru[pos];
-            if (s >= 0 && s < hot_size) {
-                const int32_t cg = dgi[s];
-                if (cg >= 0) {
-                    const int h = find_key(keys, cg, a.hash_log2);
-                    if (h >= 0) {
-                        const int i = vals[h];
-                        out[i] = int32_t(hot_base + s);
-                        state[i] = kDone;
-                        hit = 1;
-                    }
-                }
-            }
-        }
-        int tot;
-        const int excl = hs::block_excl_scan(hit, scan_scratch, &tot);
-        if (pos < hot_size) {
-            if (hit) H[hits_total + excl] = s;
-            else E[pos - (hits_total + excl)] = s;
-        }
-        hits_total += tot;
+    // Phase 2: LRU walk, least -> most recently used.  Thread t owns the
+    // contiguous positions [t*K2, t*K2 + K2); one block scan orders hits and
+    // evictables exactly as a sequential walk would.
+    const int K2 = (hot_size + kThreads - 1) / kThreads;  // <= 32
+    uint32_t hitmask = 0;
+    int nh = 0;
+    const int p0 = tid * K2;
+    for (int k = 0; k < K2; ++k) {
+        const int pos = p0 + k;
+        if (pos >= hot_size) break;
+        const int16_t sl = s_lru[pos];
+        if (sl < 0 || sl >= hot_size) continue;
+        const int32_t cg = s_dgi[sl];
+        if (cg < 0) continue;
+        const int h = find_key(keys, cg, a.hash_log2);
+        if (h < 0) continue;
+        const int i = vals[h];
+        out[i] = int32_t(hot_base + sl);
+        if (hidx) hidx[i] = int32_t(hot_base + sl);
+        state[i] = kDone;
+        hitmask |= 1u << k;
+        ++nh;
     }
+    int hits_total;
+    const int hexcl = hs::block_excl_scan(nh, scan_scratch, &hits_total);
+    {
+        int hp = hexcl, ep = min(p0, hot_size) - hexcl;
+        for (int k = 0; k < K2; ++k) {
+            const int pos = p0 + k;
+            if (pos >= hot_size) break;
+            const int16_t sl = s_lru[pos];
+            if ((hitmask >> k) & 1u) H[hp++] = sl; else E[ep++] = sl;
+        }
+    }
+    __syncthreads();
     const int nE = hot_size - hits_total;
 
-    // Phase 3: misses in row order take E[0], E[1], ...
-    int miss_total = 0;
-    for (int base = 0; base < cap; base += kThreads) {
-        const int i = base + tid;
-        const int32_t g = i < cap ? state[i] : kDone;
-        const int is_miss = g != kDone;
-        int tot;
-        const int excl = hs::block_excl_scan(is_miss, scan_scratch, &tot);
-        if (is_miss) {
-            const int m = miss_total + excl;
-            const int16_t s = m < nE ? E[m] : int16_t(-1);
-            if (s >= 0 && s < hot_size) {
-                out[i] = int32_t(hot_base + s);
-                if (mm) mm[i] = 1;
-                dgi[s] = g;
-                msrc[m] = g;
-                mdst[m] = hot_base + s;
-            } else {
-                out[i] = -1;  // only reachable with a corrupted LRU list
-            }
+    // Phase 3: misses in row order take E[0], E[1], ...  Thread t owns the
+    // contiguous entries [t*K3, t*K3 + K3).
+    const int K3 = (cap + kThreads - 1) / kThreads;
+    const int i0 = tid * K3;
+    int nm = 0;
+    for (int k = 0; k < K3; ++k) {
+        const int i = i0 + k;
+        if (i >= cap) break;
+        nm += state[i] != kDone;
+    }
+    int miss_total;
+    int m = hs::block_excl_scan(nm, scan_scratch, &miss_total);
+    for (int k = 0; k < K3; ++k) {
+        const int i = i0 + k;
+        if (i >= cap) break;
+        const int32_t g = state[i];
+        if (g == kDone) continue;
+        const int16_t sl = m < nE ? E[m] : int16_t(-1);
+        if (hidx) hidx[i] = -1;
+        if (sl >= 0 && sl < hot_size) {
+            out[i] = int32_t(hot_base + sl);
+            if (mm) mm[i] = 1;
+            dgi[sl] = g;
+            msrc[m] = g;
+            mdst[m] = hot_base + sl;
+            if (mrow) mrow[m] = int32_t(hot_base + sl);
+        } else {
+            out[i] = -1;  // only reachable with a corrupted LRU list
         }
-        miss_total += tot;
+        ++m;
     }
     const int M = min(miss_total, nE);
 
     // Phase 4: new LRU order = E[M:] ++ E[:M] ++ hits.
     for (int j = tid; j < hot_size; j += kThreads) {
-        int16_t s;
-        if (j < nE - M) s = E[M + j];
-        else if (j < nE) s = E[j - (nE - M)];
-        else s = H[j - nE];
-        lru[j] = s;
+        int16_t sl;
+        if (j < nE - M) sl = E[M + j];
+        else if (j < nE) sl = E[j - (nE - M)];
+        else sl = H[j - nE];
+        lru[j] = sl;
     }
     if (tid == 0) {
         a.miss_count[row] = M;
@@ -251,7 +283,7 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
                                     int32_t hot_size, int64_t region_stride, int32_t* hot_idx,
                                     uint8_t* miss_mask, int32_t* miss_src, int64_t* miss_dst,
                                     int32_t* miss_count, int64_t* stats, int32_t* err,
-                                    hs_stream_t stream) {
+                                    int32_t* hit_idx, int32_t* miss_rows, hs_stream_t stream) {
     if (rows < 0 || cap < 0 || hot_size <= 0 || hot_size > 32767 || num_real_rows < 0)
         return HS_ERR_INVALID_ARG;
     if (region_stride < int64_t(hot_size) + 1) return HS_ERR_INVALID_ARG;
@@ -265,7 +297,7 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
     int log2n = 6;
     while ((1 << log2n) < 2 * cap) ++log2n;
     const size_t smem = size_t(8) * (size_t(1) << log2n) + size_t(4) * cap +
-                        size_t(4) * hot_size;
+                        size_t(10) * hot_size;
     if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(lookup_kernel),
@@ -273,7 +305,8 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
     if (rc != HS_OK) return rc;
     LookupArgs a{slot,     count,    rows,     cap,        num_real_rows, newest_slot,
                  dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
-                 miss_src, miss_dst, miss_count, stats,    err,           log2n};
+                 miss_src, miss_dst, miss_count, stats,    err,           log2n,
+                 hit_idx,  miss_rows};
     lookup_kernel<<<rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();
 }

@@ -7,7 +7,9 @@
 // walkthrough, "_convert_req_index_to_global_index_kernel": slot = table[b] *
 // B + t mod B, invalid tokens propagate as -1.
 //
-// GB300 design: one CTA per index row.  Membership is a bitmap over the
+// GB300 design: one CTA per index row.  The request's block-table row is
+// copied to shared memory once (rows up to 16384 blocks), so the per-token
+// page lookups never wait on global memory.  Membership is a bitmap over the
 // row's positions in shared memory (a counting sort): W u A and then D are
 // set with atomicOr (the returned old word tells a duplicate), and the
 // ascending, de-duplicated output comes from a block-wide scan of the
@@ -23,6 +25,8 @@ constexpr int kThreads = 512;
 constexpr int kWordsPerThread = 8;
 constexpr int kWindowWords = kThreads * kWordsPerThread;     // 4096 words = 16 KB
 constexpr int64_t kWindowBits = int64_t(kWindowWords) * 32;  // 131072 positions
+constexpr int kMaxStagedBlocks = 16384;  // block-table rows up to this are copied to smem
+constexpr int kUnroll = 4;               // candidates loaded per thread before use
 
 struct NormArgs {
     const int32_t* cand;
@@ -38,6 +42,7 @@ struct NormArgs {
     int32_t* out_slot;
     int32_t* out_count;
     int32_t* err_counts;
+    int32_t stage_table;  // 1: the request's block-table row is staged in shared memory
 };
 
 // Checks of a position already known to satisfy 0 <= t < T.
@@ -46,13 +51,14 @@ __device__ __forceinline__ int classify_in_range(int64_t t, const int32_t* table
                                                  const NormArgs& a, int32_t req) {
     const int64_t b = t / a.page_size;
     if (b >= a.max_blocks) return 0;
-    const int32_t p = __ldg(table + b);
+    const int32_t p = table[b];
     if (p < 0 || p >= a.num_pages) return 0;
     if (a.page_owner != nullptr && __ldg(a.page_owner + p) != req) return 2;
     return -1;
 }
 
 __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
+    extern __shared__ int32_t s_table[];  // [max_blocks] when a.stage_table
     __shared__ uint32_t bm[kWindowWords];
     __shared__ int scan_scratch[33];
     __shared__ int s_err[4];
@@ -75,17 +81,32 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
     } else {
         const int64_t T = max(a.seq_lens[req], 0);
         const int32_t* table = a.block_table + int64_t(req) * a.bt_stride;
+        if (a.stage_table) {
+            // One coalesced copy of the row; every later lookup hits shared memory.
+            for (int b = tid; b < a.max_blocks; b += kThreads) s_table[b] = __ldg(table + b);
+            __syncthreads();
+            table = s_table;
+        }
         const int64_t a_hi = hs::min64(a.num_sinks, T);        // sinks  [0, a_hi)
         const int64_t s2 = hs::max64(hs::max64(T - a.window, 0), a_hi);  // window [s2, T)
 
         // Dynamic candidates outside [0, T) are rejected once, before the windows.
         {
             int er = 0, ec = 0;
-            for (int i = tid; i < a.n_cand; i += kThreads) {
-                const int32_t t = cand[i];
-                if (t == -1) continue;
-                if (t < 0) ++er;
-                else if (t >= T) ++ec;
+            for (int i0 = tid; i0 < a.n_cand; i0 += kThreads * kUnroll) {
+                int32_t tv[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int i = i0 + u * kThreads;
+                    tv[u] = i < a.n_cand ? __ldg(cand + i) : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int32_t t = tv[u];
+                    if (t == -1) continue;
+                    if (t < 0) ++er;
+                    else if (t >= T) ++ec;
+                }
             }
             if (er) atomicAdd(&s_err[0], er);
             if (ec) atomicAdd(&s_err[1], ec);
@@ -115,17 +136,26 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
                 }
             }
             __syncthreads();
-            // Dynamic candidates inside this window.
-            for (int i = tid; i < a.n_cand; i += kThreads) {
-                const int64_t t = cand[i];
-                if (t < lo || t >= hi) continue;
-                const int c = classify_in_range(t, table, a, req);
-                if (c == 0) { ++er; continue; }
-                if (c == 2) { ++eo; continue; }
-                const int64_t o = t - lo;
-                const uint32_t bit = 1u << (o & 31);
-                const uint32_t old = atomicOr(&bm[o >> 5], bit);
-                if (old & bit) ++ed;
+            // Dynamic candidates inside this window (kUnroll independent loads first).
+            for (int i0 = tid; i0 < a.n_cand; i0 += kThreads * kUnroll) {
+                int32_t tv[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int i = i0 + u * kThreads;
+                    tv[u] = i < a.n_cand ? __ldg(cand + i) : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int64_t t = tv[u];
+                    if (t < lo || t >= hi) continue;
+                    const int c = classify_in_range(t, table, a, req);
+                    if (c == 0) { ++er; continue; }
+                    if (c == 2) { ++eo; continue; }
+                    const int64_t o = t - lo;
+                    const uint32_t bit = 1u << (o & 31);
+                    const uint32_t old = atomicOr(&bm[o >> 5], bit);
+                    if (old & bit) ++ed;
+                }
             }
             if (er) atomicAdd(&s_err[0], er);
             if (eo) atomicAdd(&s_err[2], eo);
@@ -151,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
                     const int b = __ffs(x) - 1;
                     x &= x - 1;
                     const int64_t t = base + b;
-                    const int64_t p = __ldg(table + t / a.page_size);
+                    const int64_t p = table[t / a.page_size];
                     otok[pos] = int32_t(t);
                     oslot[pos] = int32_t(p * a.page_size + t % a.page_size);
                     ++pos;
@@ -194,7 +224,12 @@ extern "C" int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n
     NormArgs a{cand,      rows,      n_cand,     window,    num_sinks, row_req,
                seq_lens,  block_table, bt_stride, max_blocks, page_owner, num_reqs,
                num_pages, page_size, cap,        out_tok,   out_slot,  out_count,
-               err_counts};
-    normalize_kernel<<<rows, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+               err_counts, max_blocks <= kMaxStagedBlocks ? 1 : 0};
+    const size_t smem = a.stage_table ? size_t(max_blocks) * sizeof(int32_t) : 0;
+    static int smem_set[64] = {};
+    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(normalize_kernel),
+                                                smem, smem_set);
+    if (rc != HS_OK) return rc;
+    normalize_kernel<<<rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();
 }

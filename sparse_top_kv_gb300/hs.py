@@ -37,7 +37,7 @@ _SIGS = {
                               _I32, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "hs_hot_state_reset": ([_P, _P, _I32, _I32, _P], ctypes.c_int),
     "hs_hot_lookup_assign": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
-                              _P, _P, _P, _P], ctypes.c_int),
+                              _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _P, _P],
                    ctypes.c_int),
     "hs_backup": ([_P, _P, _P, _P, _I32, _I64, _I64, _P, _P], ctypes.c_int),
@@ -45,6 +45,10 @@ _SIGS = {
     "hs_sparse_decode": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32,
                           _I32, _F32, _P, _P, _P, _I64, _P, _P], ctypes.c_int),
     "hs_merge_states": ([_P, _P, _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "hs_sparse_decode_partial_splits": ([_I32, _I32, _I32, _I32, _I32, _I32], _I32),
+    "hs_sparse_decode_partial": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
+                                  _I32, _I32, _F32, _P, _P, _P, _I32, _I32, _P, _P],
+                                 ctypes.c_int),
     "hs_sparse_decode_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
                                   _I32, _I32, _F32, _P, _P, _P, _P], ctypes.c_int),
 }
@@ -145,9 +149,11 @@ def hot_state_reset(dgi, lru, stream=None):
 
 
 def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, *,
-                      num_real_rows=None, out=None, with_mask=True, stream=None):
+                      num_real_rows=None, out=None, with_mask=True, with_split_lists=False,
+                      stream=None):
     """S2.  dgi/lru are updated in place; stats int64 [2] accumulates.
-    Returns (hot_idx, miss_mask, miss_src, miss_dst, miss_count, err)."""
+    Returns (hot_idx, miss_mask, miss_src, miss_dst, miss_count, err) and, with
+    with_split_lists (or an 8-tuple `out`), also (hit_idx, miss_rows)."""
     _check(slot, torch.int32, "slot")
     _check(count, torch.int32, "count")
     _check(newest_slot, torch.int32, "newest_slot")
@@ -164,12 +170,16 @@ def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, 
                torch.empty(rows, cap, dtype=torch.int64, device=dev),
                torch.empty(rows, dtype=torch.int32, device=dev),
                torch.empty(rows, dtype=torch.int32, device=dev))
-    hot_idx, miss_mask, miss_src, miss_dst, miss_count, err = out
+        if with_split_lists:
+            out = out + (torch.empty(rows, cap, dtype=torch.int32, device=dev),
+                         torch.empty(rows, cap, dtype=torch.int32, device=dev))
+    hot_idx, miss_mask, miss_src, miss_dst, miss_count, err = out[:6]
+    hit_idx, miss_rows = (out[6], out[7]) if len(out) == 8 else (None, None)
     nrr = rows if num_real_rows is None else num_real_rows
     _call("hs_hot_lookup_assign", _ptr(slot), _ptr(count), rows, cap, nrr, _ptr(newest_slot),
           _ptr(dgi), _ptr(lru), hot_size, region_stride, _ptr(hot_idx), _ptr(miss_mask),
           _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), _ptr(stats), _ptr(err),
-          _stream(stream))
+          _ptr(hit_idx), _ptr(miss_rows), _stream(stream))
     return out
 
 
@@ -225,6 +235,32 @@ def sparse_decode(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv
           workspace.numel() * workspace.element_size() if (ws > 0) else 0, _ptr(status),
           _stream(stream))
     return out, lse
+
+
+def sparse_decode_partial_splits(rows, heads, kv_heads, cap, d_qk, d_v):
+    return int(lib().hs_sparse_decode_partial_splits(rows, heads, kv_heads, cap, d_qk, d_v))
+
+
+def sparse_decode_partial(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows,
+                          count, scale, d_v, part_m, part_l, part_o, part_base, *, status=None,
+                          stream=None):
+    """S4 partial states into columns [part_base, part_base + P) of
+    part_m/part_l fp32 [rows*heads, parts] and part_o fp32 [rows*heads, parts, d_v];
+    returns P.  Combine with merge_states."""
+    _check(q, torch.bfloat16, "q")
+    _check(kv_rows, torch.int32, "kv_rows")
+    _check(count, torch.int32, "count")
+    for t, n in ((part_m, "part_m"), (part_l, "part_l"), (part_o, "part_o")):
+        _check(t, torch.float32, n)
+    _check(status, torch.int32, "status")
+    rows, heads, d_qk = q.shape
+    _, kv_heads, cap = kv_rows.shape
+    parts = part_m.shape[-1]
+    _call("hs_sparse_decode_partial", _ptr(q), _ptr(k_base), _ptr(v_base), row_stride,
+          kv_head_stride, num_kv_rows, _ptr(kv_rows), _ptr(count), rows, cap, heads, kv_heads,
+          d_qk, d_v, float(scale), _ptr(part_m), _ptr(part_l), _ptr(part_o), parts, part_base,
+          _ptr(status), _stream(stream))
+    return sparse_decode_partial_splits(rows, heads, kv_heads, cap, d_qk, d_v)
 
 
 def merge_states(m, l, o, *, out=None, lse=None, stream=None):

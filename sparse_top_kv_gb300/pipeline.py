@@ -57,11 +57,23 @@ class HiSparseDecoder:
                        torch.empty(R, cap, dtype=torch.uint8, device=dev),
                        torch.empty(R, cap, **i32),
                        torch.empty(R, cap, dtype=torch.int64, device=dev),
-                       torch.empty(R, **i32), torch.empty(R, **i32))
+                       torch.empty(R, **i32), torch.empty(R, **i32),
+                       torch.empty(R, cap, **i32), torch.empty(R, cap, **i32))
         self.out = torch.empty(R, heads, d_v, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(R, heads, dtype=torch.float32, device=dev)
         ws = hs.sparse_decode_workspace_bytes(R, heads, 1, cap, d_qk, d_v)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        # Partial states of the two attention passes (resident rows, swapped rows).
+        self.parts_hit = hs.sparse_decode_partial_splits(R, heads, 1, cap, d_qk, d_v)
+        self.parts_miss = self.parts_hit
+        P = self.parts_hit + self.parts_miss
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.part_m = torch.empty(R * heads, P, **f32)
+        self.part_l = torch.empty(R * heads, P, **f32)
+        self.part_o = torch.empty(R * heads, P, d_v, **f32)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_lists = torch.cuda.Event()
+        self.ev_swapped = torch.cuda.Event()
 
     def warm_pool(self, page_bytes=65536):
         """One-time set-up pass: read one row of every `page_bytes` of the host
@@ -96,42 +108,66 @@ class HiSparseDecoder:
         """cand int32 [R, top_k] positions; seq_lens int32 [R]; newest_slot int32
         [R]; new_row [R, row_width] (the new token's KV row); q bf16 [R, H, d_qk].
         Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated.
-        `events`, if given, is a list of 6 CUDA events recorded before S1 and
-        after S1, S2, SwapIn, BackUp and S4."""
+
+        The SwapIn and BackUp run on a side stream, concurrently with the
+        attention over the rows that were already resident (hit_idx); the
+        attention over the swapped rows (miss_rows) follows the SwapIn, and the
+        two sets of partial states are merged with eq. (7).
+        `events`, if given, is a list of 7 CUDA events recorded before S1, after
+        S1, after S2, after SwapIn (side), after BackUp (side), after the
+        resident-row attention and at the end of the step."""
         R = self.num_reqs
-        rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        side = self.side
+        rec = (lambda i, st: events[i].record(st)) if events is not None else (lambda i, st: None)
         # The model's KV write of the newest token (stand-in): reserved hot rows.
-        self.hot.index_copy_(0, self.reserved_rows, new_row)
-        rec(0)
+        with torch.cuda.stream(main):
+            self.hot.index_copy_(0, self.reserved_rows, new_row)
+        rec(0, main)
         tok, slot, count, err = hs.normalize_indices(
             cand, self.row_req, seq_lens, self.block_table, self.page_size,
             window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
-            out=self.s1_out, stream=stream)
-        rec(1)
-        hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr = hs.hot_lookup_assign(
-            slot, count, newest_slot, self.dgi, self.lru, self.region_stride, self.stats,
-            out=self.s2_out, stream=stream)
-        rec(2)
+            out=self.s1_out, stream=main)
+        rec(1, main)
+        (hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr, hit_idx,
+         miss_rows) = hs.hot_lookup_assign(slot, count, newest_slot, self.dgi, self.lru,
+                                           self.region_stride, self.stats, out=self.s2_out,
+                                           stream=main)
+        rec(2, main)
+        self.ev_lists.record(main)
+        # Side stream: host link traffic.
+        side.wait_event(self.ev_lists)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
-                   region_stride=self.region_stride, status=self.status, stream=stream)
-        rec(3)
+                   region_stride=self.region_stride, status=self.status, stream=side)
+        rec(3, side)
         hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
-                  self.host_rows, status=self.status, stream=stream)
-        rec(4)
-        hs.sparse_decode(self.q_view(q), self.hot, self.hot, self.row_width, 0, self.hot.shape[0],
-                         hot_idx.view(R, 1, self.cap), count.view(R, 1), self.scale, self.d_v,
-                         out=self.out, lse=self.lse, workspace=self.workspace,
-                         status=self.status, stream=stream)
-        rec(5)
+                  self.host_rows, status=self.status, stream=side)
+        rec(4, side)
+        self.ev_swapped.record(side)
+        # Main stream: HBM traffic over the resident rows meanwhile.
+        qv = self.q_view(q)
+        nkv = self.hot.shape[0]
+        hs.sparse_decode_partial(qv, self.hot, self.hot, self.row_width, 0, nkv,
+                                 hit_idx.view(R, 1, self.cap), count.view(R, 1), self.scale,
+                                 self.d_v, self.part_m, self.part_l, self.part_o, 0,
+                                 status=self.status, stream=main)
+        rec(5, main)
+        main.wait_event(self.ev_swapped)
+        hs.sparse_decode_partial(qv, self.hot, self.hot, self.row_width, 0, nkv,
+                                 miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),
+                                 self.scale, self.d_v, self.part_m, self.part_l, self.part_o,
+                                 self.parts_hit, status=self.status, stream=main)
+        hs.merge_states(self.part_m, self.part_l, self.part_o, out=self.out.view(R * self.heads, -1),
+                        lse=self.lse.view(-1), stream=main)
+        rec(6, main)
         return self.out, self.lse
 
     @staticmethod
     def q_view(q):
         return q if q.dtype == torch.bfloat16 else q.view(torch.bfloat16)
 
-    # Kernels of libhs launched by one step (index_copy_ above is torch's).
+    # Kernels of libhs launched by one step (index_copy_ above is torch's):
+    # S1, S2, SwapIn, BackUp, two attention passes, merge.
     def launches_per_step(self):
-        ws = hs.sparse_decode_workspace_bytes(self.num_reqs, self.heads, 1, self.cap, self.d_qk,
-                                              self.d_v)
-        return 5 + (1 if ws > 0 else 0)
+        return 7

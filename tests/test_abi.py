@@ -44,8 +44,10 @@ def test_host_side_argument_checks():
     assert L.hs_normalize_indices(P, 1, 4, 2, 1, P, P, P, 4, 4, P, 1, 1, 64, 6, P, P, P, P,
                                   P) == 3
     # cap > hot_size, region stride too small, hot_size beyond int16 slots.
-    assert L.hs_hot_lookup_assign(P, P, 1, 9, 1, P, P, P, 8, 9, P, P, P, P, P, P, P, P) == 3
-    assert L.hs_hot_lookup_assign(P, P, 1, 4, 1, P, P, P, 8, 8, P, P, P, P, P, P, P, P) == 1
+    assert L.hs_hot_lookup_assign(P, P, 1, 9, 1, P, P, P, 8, 9, P, P, P, P, P, P, P, P, P,
+                                  P) == 3
+    assert L.hs_hot_lookup_assign(P, P, 1, 4, 1, P, P, P, 8, 8, P, P, P, P, P, P, P, P, P,
+                                  P) == 1
     assert L.hs_hot_state_reset(P, P, 1, 40000, P) == 1
     # Rows not a multiple of 16 bytes.
     assert L.hs_swap_in(P, 10, P, 100, P, P, P, 1, 1, P, 0, 0, P, P) == 2
@@ -58,6 +60,11 @@ def test_host_side_argument_checks():
     assert L.hs_sparse_decode(P, p, p, 576, 0, 10, p, P, 1, 4, 4, 1, 576, 512, 1.0, p, P, P, 0,
                               P, P) == 1
     assert L.hs_merge_states(P, P, P, 1, 0, 8, P, P, P) == 1
+    # Partial states: null outputs, and columns beyond parts_total.
+    assert L.hs_sparse_decode_partial(p, p, p, 576, 0, 10, p, P, 1, 4, 16, 1, 576, 512, 1.0, P,
+                                      P, P, 1, 0, P, P) == 1
+    assert L.hs_sparse_decode_partial(p, p, p, 576, 0, 10, p, P, 1, 4, 16, 1, 576, 512, 1.0, p,
+                                      p, p, 1, 1, P, P) == 1
 
 
 @pytest.mark.parametrize("rows,heads,cap", [(32, 128, 2048), (64, 16, 2048), (1, 16, 64)])

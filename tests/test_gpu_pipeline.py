@@ -48,7 +48,15 @@ def run_steps(cfg, pool, attend_sample=None, steps=None):
         tok, slot, count, err = dec.s1_out
         for name, g in (("tok", tok), ("slot", slot), ("count", count), ("err", err)):
             np.testing.assert_array_equal(np_i32(g), ref[name], err_msg=f"step {s} {name}")
-        hot_idx, mm, msrc, mdst, mcount, lerr = dec.s2_out
+        hot_idx, mm, msrc, mdst, mcount, lerr, hit_idx, miss_rows = dec.s2_out
+        # The split lists: resident rows keep their hot row, the swapped ones
+        # are listed compactly.
+        exp_hit = np.where(ref["miss_mask"] == 0, ref["hot_idx"], -1)
+        np.testing.assert_array_equal(np_i32(hit_idx), exp_hit, err_msg=f"step {s} hit_idx")
+        for r in range(R):
+            m = int(ref["miss_count"][r])
+            np.testing.assert_array_equal(np_i32(miss_rows)[r, :m], ref["miss_dst"][r, :m])
+            assert (np_i32(miss_rows)[r, m:] == -1).all()
         for name, g in (("hot_idx", hot_idx), ("miss_mask", mm), ("miss_count", mcount),
                         ("lookup_err", lerr)):
             np.testing.assert_array_equal(np_i32(g), ref[name], err_msg=f"step {s} {name}")

@@ -39,12 +39,19 @@ class Pair:
         got = hs.hot_lookup_assign(cuda(slot), None if count is None else cuda(count),
                                    None if newest is None else cuda(newest), self.gdgi,
                                    self.glru, self.region, self.gstats,
-                                   num_real_rows=num_real_rows)
+                                   num_real_rows=num_real_rows, with_split_lists=True)
         torch.cuda.synchronize()
         names = ("hot_idx", "miss_mask", "miss_src", "miss_dst", "miss_count")
         for name, r, g in zip(names, ref[:5], got[:5]):
             np.testing.assert_array_equal(np_i32(g), r, err_msg=name)
         np.testing.assert_array_equal(np_i32(got[5]), ref[6], err_msg="err")
+        np.testing.assert_array_equal(np_i32(got[6]), np.where(ref[1] == 0, ref[0], -1),
+                                      err_msg="hit_idx")
+        mr = np_i32(got[7])
+        for r in range(slot.shape[0]):
+            m = int(ref[4][r])
+            np.testing.assert_array_equal(mr[r, :m], ref[3][r, :m], err_msg="miss_rows")
+            assert (mr[r, m:] == -1).all()
         np.testing.assert_array_equal(np_i32(self.gdgi), self.dgi, err_msg="dgi")
         np.testing.assert_array_equal(np_i32(self.glru), self.lru, err_msg="lru")
         np.testing.assert_array_equal(np_i32(self.gstats), self.stats, err_msg="stats")

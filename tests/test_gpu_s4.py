@@ -108,6 +108,62 @@ def test_out_of_range_rows_flagged_and_skipped():
     check_attention(out, lse, ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("heads,d", [(16, 576), (128, 576), (4, 128)])
+def test_partial_passes_merge_to_the_full_set(heads, d):
+    """Two partial passes over disjoint halves of each candidate list (as the
+    pipeline does for resident and swapped rows), merged by eq. (7), equal
+    the oracle over the whole list."""
+    rng = np.random.default_rng(heads + d)
+    rows, n_kv, cap = 40, 5000, 700
+    mla = d == 576
+    kv_heads = 1 if mla else 2
+    q = inputs.randn_bf16((rows, heads * (1 if mla else kv_heads), d), 90, device="cuda")
+    H = q.shape[1]
+    if mla:
+        k = v = inputs.randn_bf16((n_kv, 576), 91, device="cuda")
+        rs, hsd, d_v = 576, 0, 512
+    else:
+        k = inputs.randn_bf16((n_kv, kv_heads, d), 92, device="cuda")
+        v = inputs.randn_bf16((n_kv, kv_heads, d), 93, device="cuda")
+        rs, hsd, d_v = kv_heads * d, d, d
+    full, count = random_sets(rng, rows, kv_heads, cap, n_kv)
+    a = np.full_like(full, -1)
+    b = np.full_like(full, -1)
+    ca = np.zeros_like(count)
+    cb = np.zeros_like(count)
+    for r in range(rows):
+        for g in range(kv_heads):
+            n = count[r, g]
+            sel = rng.random(n) < 0.8
+            ia = full[r, g, :n][sel]
+            ib = full[r, g, :n][~sel]
+            a[r, g, :n] = np.where(sel, full[r, g, :n], -1)  # in place, holes elsewhere
+            b[r, g, :len(ib)] = ib                           # compact
+            ca[r, g], cb[r, g] = n, len(ib)
+    pa = hs.sparse_decode_partial_splits(rows, H, kv_heads, cap, d, d_v)
+    pb = hs.sparse_decode_partial_splits(rows, H, kv_heads, cap, d, d_v)
+    P = pa + pb + 1
+    pm = torch.full((rows * H, P), -np.inf, dtype=torch.float32, device="cuda")
+    pl = torch.zeros(rows * H, P, dtype=torch.float32, device="cuda")
+    po = torch.zeros(rows * H, P, d_v, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nkv = k.numel() // rs
+    assert hs.sparse_decode_partial(q, k, v, rs, hsd, nkv, cuda(a), cuda(ca), 1 / math.sqrt(d),
+                                    d_v, pm, pl, po, 0, status=status) == pa
+    hs.sparse_decode_partial(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb), 1 / math.sqrt(d), d_v,
+                             pm, pl, po, pa, status=status)
+    out, lse = hs.merge_states(pm, pl, po)  # the extra empty column (l = 0) is skipped
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    sample = [0, 7, rows - 1]
+    kb = bits(k).reshape(-1)
+    vb = kb if mla else bits(v).reshape(-1)
+    ref_out, ref_lse = oracle.sparse_decode(bits(q)[sample], kb, vb, rs, hsd, full[sample],
+                                            count[sample], 1 / math.sqrt(d), d_v=d_v)
+    idx = torch.tensor(sample, device="cuda")
+    check_attention(out.view(rows, H, d_v)[idx], lse.view(rows, H)[idx], ref_out, ref_lse)
+
+
 def test_merge_states_kernel():
     rng = np.random.default_rng(12)
     n, parts, d = 37, 5, 512
