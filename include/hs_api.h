@@ -149,8 +149,9 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
 /* ---------------------------------------------------------------------------
  * S3  hs_swap_in -- [HS] Phase 5 (copy each miss row host -> hot; a source
  * outside [0, host_rows) zeroes the hot row and revokes its slot, dgi = -1),
- * [HC] Modifications (TMA bulk copies staged through a shared-memory ring,
- * one bulk op per contiguous run, per-row ops for scattered rows).
+ * [HC] Modifications (copies staged through a shared-memory ring; one TMA
+ * bulk op per contiguous run).  Scattered rows are staged with 16-byte
+ * cp.async by whole warps instead of per-row bulk ops.
  *
  * host_pool   device-visible pointer to the pinned host pool, host_rows rows
  *             of row_bytes each (16-byte aligned base).
@@ -158,6 +159,11 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
  * row_bytes   multiple of 16 ([HS] HiSparseCoordinator rejects others).
  * miss_src/miss_dst/miss_count  as produced by hs_hot_lookup_assign.
  * dgi         int32 [rows, hot_size] or NULL: revocation target.
+ * max_ctas    CTAs the copy may occupy (0 = two per SM).  A smaller budget
+ *             leaves SMs to a kernel running concurrently on another stream
+ *             ([HC] Motivation: the copy's SM footprint is the cost to the
+ *             concurrent forward pass); a few dozen CTAs already keep enough
+ *             bytes in flight to fill the host link.
  * status      int32 device word or NULL: HS_ERR_TIMEOUT / HS_ERR_BAD_INDEX
  *             is stored there (first error wins) if the device hits one.
  * Destinations must be distinct within one call.
@@ -165,7 +171,7 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
 int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, int64_t row_bytes,
                const int32_t* miss_src, const int64_t* miss_dst, const int32_t* miss_count,
                int32_t rows, int32_t cap, int32_t* dgi, int32_t hot_size, int64_t region_stride,
-               int32_t* status, hs_stream_t stream);
+               int32_t max_ctas, int32_t* status, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hs_backup -- [HS] overview "BackUp": after each step copy the newly
@@ -246,6 +252,24 @@ int hs_sparse_decode_partial(const void* q, const void* k_base, const void* v_ba
                              int32_t d_v, float scale, float* part_m, float* part_l,
                              float* part_o, int32_t parts_total, int32_t part_base,
                              int32_t* status, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hs_sparse_decode_finish -- the last pass of a split computation: attend over
+ * kv_rows, merge (eq. 7) with the partial states already in columns
+ * [0, parts_used) of part_m / part_l / part_o (written by
+ * hs_sparse_decode_partial), and write the final out (bf16 [rows, heads, d_v])
+ * and lse (fp32 [rows, heads], natural log, or NULL).  Columns
+ * [parts_used, parts_total) may be used as scratch: parts_total must be at
+ * least parts_used + hs_sparse_decode_partial_splits(...).  For the MLA shape
+ * the merge runs in the attention kernel's epilogue (no extra launch).
+ * ------------------------------------------------------------------------- */
+int hs_sparse_decode_finish(const void* q, const void* k_base, const void* v_base,
+                            int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
+                            const int32_t* kv_rows, const int32_t* count, int32_t rows,
+                            int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
+                            int32_t d_v, float scale, float* part_m, float* part_l,
+                            float* part_o, int32_t parts_total, int32_t parts_used, void* out,
+                            float* lse, int32_t* status, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hs_sparse_decode_noalloc -- the paper has no counterpart; this is a

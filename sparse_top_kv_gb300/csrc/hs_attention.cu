@@ -246,10 +246,11 @@ __global__ void __launch_bounds__(kThreads) attn_cc_kernel(const AttnArgs a) {
 // Eq. (7) over `parts` partial states per output row; m in log2 units.
 __global__ void merge_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                              const float* __restrict__ po, int32_t parts, int32_t d_v,
-                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                             int32_t stride) {
     const int64_t n = blockIdx.x;
-    const float* m = pm + n * parts;
-    const float* l = pl + n * parts;
+    const float* m = pm + n * stride;
+    const float* l = pl + n * stride;
     float M = -CUDART_INF_F;
     for (int p = 0; p < parts; ++p)
         if (l[p] > 0.f) M = fmaxf(M, m[p]);
@@ -262,7 +263,7 @@ __global__ void merge_kernel(const float* __restrict__ pm, const float* __restri
         float O = 0.f;
         if (M != -CUDART_INF_F)
             for (int p = 0; p < parts; ++p)
-                if (l[p] > 0.f) O = fmaf(exp2f(m[p] - M), po[(n * parts + p) * d_v + d], O);
+                if (l[p] > 0.f) O = fmaf(exp2f(m[p] - M), po[(n * stride + p) * d_v + d], O);
         out[n * d_v + d] = __float2bfloat16_rn(O * inv);
     }
     if (threadIdx.x == 0 && lse != nullptr)
@@ -354,6 +355,7 @@ struct PartialOut {
     float* o;
     int32_t parts_total;
     int32_t part_base;
+    int32_t finish;  // 1: merge with columns [0, part_base) and write out / lse
 };
 
 int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t row_stride,
@@ -378,16 +380,27 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
     if (p.kind == 0) return HS_ERR_UNSUPPORTED;
     const int64_t n = int64_t(rows) * heads;
     AttnArgs a{};
+    int combine = 0;
+    Plan pl = p;
     if (po != nullptr) {
         if (po->m == nullptr || po->l == nullptr || po->o == nullptr || po->part_base < 0 ||
-            po->part_base + p.splits > po->parts_total)
+            po->part_base > po->parts_total)
             return HS_ERR_INVALID_ARG;
+        if (po->finish && pl.kind == 3 && po->part_base <= 4) {
+            // One CTA per row and head group; its epilogue merges.
+            pl.splits = 1;
+            combine = po->part_base;
+            if (out == nullptr) return HS_ERR_INVALID_ARG;
+        } else if (po->part_base + p.splits > po->parts_total) {
+            return HS_ERR_INVALID_ARG;
+        }
         a.part_m = po->m;
         a.part_l = po->l;
         a.part_o = po->o;
         a.part_stride = po->parts_total;
         a.part_base = po->part_base;
-        a.force_partial = 1;
+        const bool fused = po->finish && pl.kind == 3 && po->part_base <= 4;
+        a.force_partial = fused ? 0 : 1;
     } else {
         const int64_t ws = workspace_bytes(p, rows, heads, d_v);
         if (ws > 0 && (workspace == nullptr || workspace_bytes_given < ws)) return HS_ERR_CAPACITY;
@@ -418,7 +431,7 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
     a.scale_log2 = scale * kLog2e;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
-    a.splits = p.splits;
+    a.splits = pl.splits;
     a.chunks_per_kvh = p.chunks_per_kvh;
     a.status = status;
     const int units = rows * kv_heads * p.chunks_per_kvh;
@@ -440,13 +453,14 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         m.part_m = a.part_m;
         m.part_l = a.part_l;
         m.part_o = a.part_o;
-        m.splits = p.splits;
+        m.splits = pl.splits;
         m.part_stride = a.part_stride;
         m.part_base = a.part_base;
         m.force_partial = a.force_partial;
+        m.combine_parts = combine;
         m.status = status;
         m.timeout_ns = hs::kWaitTimeoutNs;
-        rc = launch_mla_tc(m, p.G, dim3(units, p.splits), stream);
+        rc = launch_mla_tc(m, p.G, dim3(units, pl.splits), stream);
     } else if (p.kind == 1) {
         rc = launch<576, 512, 4, true, 2>(a, units, stream);
     } else {
@@ -457,9 +471,18 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
             default: rc = launch<128, 128, 8, false, 2>(a, units, stream); break;
         }
     }
-    if (rc != HS_OK || po != nullptr || p.splits == 1) return rc;
+    if (rc != HS_OK) return rc;
+    if (po != nullptr) {
+        if (!po->finish || (pl.kind == 3 && po->part_base <= 4)) return rc;
+        // Finish on the other kernels: merge every column written so far.
+        merge_kernel<<<int(n), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+            a.part_m, a.part_l, a.part_o, po->part_base + p.splits, d_v,
+            static_cast<__nv_bfloat16*>(out), lse, po->parts_total);
+        return hs_host::launch_status();
+    }
+    if (p.splits == 1) return rc;
     merge_kernel<<<int(n), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        a.part_m, a.part_l, a.part_o, p.splits, d_v, a.out, lse);
+        a.part_m, a.part_l, a.part_o, p.splits, d_v, a.out, lse, p.splits);
     return hs_host::launch_status();
 }
 
@@ -491,10 +514,25 @@ extern "C" int hs_sparse_decode_partial(const void* q, const void* k_base, const
                                         int32_t d_v, float scale, float* part_m, float* part_l,
                                         float* part_o, int32_t parts_total, int32_t part_base,
                                         int32_t* status, hs_stream_t stream) {
-    const PartialOut po{part_m, part_l, part_o, parts_total, part_base};
+    const PartialOut po{part_m, part_l, part_o, parts_total, part_base, 0};
     return decode_impl(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
                        rows, cap, heads, kv_heads, d_qk, d_v, scale, nullptr, nullptr, nullptr, 0,
                        &po, status, stream);
+}
+
+extern "C" int hs_sparse_decode_finish(const void* q, const void* k_base, const void* v_base,
+                                       int64_t row_stride, int64_t kv_head_stride,
+                                       int64_t num_kv_rows, const int32_t* kv_rows,
+                                       const int32_t* count, int32_t rows, int32_t cap,
+                                       int32_t heads, int32_t kv_heads, int32_t d_qk,
+                                       int32_t d_v, float scale, float* part_m, float* part_l,
+                                       float* part_o, int32_t parts_total, int32_t parts_used,
+                                       void* out, float* lse, int32_t* status,
+                                       hs_stream_t stream) {
+    const PartialOut po{part_m, part_l, part_o, parts_total, parts_used, 1};
+    return decode_impl(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
+                       rows, cap, heads, kv_heads, d_qk, d_v, scale, out, lse, nullptr, 0, &po,
+                       status, stream);
 }
 
 extern "C" int hs_merge_states(const float* m, const float* l, const float* o, int32_t n,
@@ -504,7 +542,7 @@ extern "C" int hs_merge_states(const float* m, const float* l, const float* o, i
     if (n == 0) return HS_OK;
     if (m == nullptr || l == nullptr || o == nullptr || out == nullptr) return HS_ERR_INVALID_ARG;
     merge_kernel<<<n, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        m, l, o, parts, d_v, static_cast<__nv_bfloat16*>(out), lse);
+        m, l, o, parts, d_v, static_cast<__nv_bfloat16*>(out), lse, parts);
     return hs_host::launch_status();
 }
 

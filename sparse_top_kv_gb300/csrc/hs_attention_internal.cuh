@@ -26,6 +26,8 @@ struct MlaArgs {
     int32_t part_stride;
     int32_t part_base;
     int32_t force_partial;    // 1: write partial states even when splits == 1
+    int32_t combine_parts;    // >0 (splits == 1): merge with partial columns [0, combine_parts)
+                              // in the epilogue and write the final out / lse
     int32_t* status;
     uint64_t timeout_ns;
 };

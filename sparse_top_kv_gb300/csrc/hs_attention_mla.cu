@@ -40,6 +40,7 @@ constexpr int kPair = 2 * kBlk;
 constexpr int kThreads = 288;       // 4 softmax + 4 loader warps + 1 MMA warp
 constexpr int kLoaderThreads = 128;
 constexpr float kThresh = 8.0f;     // log2 headroom before O is rescaled
+constexpr int kMaxCombine = 4;      // partial columns a finishing pass can merge
 
 template <int HG>
 struct Cfg {
@@ -72,6 +73,7 @@ struct Bars {
     int32_t abort;
     uint32_t vote[2][4][2];
     float red[4][64];
+    float cw[64][6];  // finishing merge, per head: w_own, 1/L_total, w_part[4]
 };
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -469,6 +471,51 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                     for (int h = 0; h < HG; ++h)
                         L[h] = B.red[0][h] + B.red[1][h] + B.red[2][h] + B.red[3][h];
                     const int64_t qh0 = int64_t(row) * a.heads + head0;
+                    // Eq. (7) with earlier partial states of the same rows (the
+                    // resident-row pass): weights of every part, per head.
+                    const int cp = min(a.combine_parts, kMaxCombine);
+                    if (cp > 0) {
+                        // Per-head merge weights, computed once (thread h) into smem.
+                        if (tid < HG) {
+                            float Lh = 0.f, Mo = -CUDART_INF_F;
+#pragma unroll
+                            for (int h = 0; h < HG; ++h)
+                                if (h == tid) { Lh = L[h]; Mo = m_ref[h]; }
+                            const int64_t base = (qh0 + tid) * a.part_stride;
+                            float mp[kMaxCombine], lp[kMaxCombine];
+                            float M = Lh > 0.f ? Mo : -CUDART_INF_F;
+#pragma unroll
+                            for (int pp = 0; pp < kMaxCombine; ++pp) {
+                                mp[pp] = pp < cp ? a.part_m[base + pp] : -CUDART_INF_F;
+                                lp[pp] = pp < cp ? a.part_l[base + pp] : 0.f;
+                                if (lp[pp] > 0.f) M = fmaxf(M, mp[pp]);
+                            }
+                            float Lt = 0.f, wo = 0.f;
+                            float* w = B.cw[tid];
+#pragma unroll
+                            for (int pp = 0; pp < kMaxCombine; ++pp) w[2 + pp] = 0.f;
+                            if (M != -CUDART_INF_F) {
+                                wo = Lh > 0.f ? exp2f(Mo - M) : 0.f;
+                                Lt = wo * Lh;
+#pragma unroll
+                                for (int pp = 0; pp < kMaxCombine; ++pp) {
+                                    if (lp[pp] > 0.f) {
+                                        w[2 + pp] = exp2f(mp[pp] - M);
+                                        Lt = fmaf(w[2 + pp], lp[pp], Lt);
+                                    }
+                                }
+                            }
+                            w[0] = wo;
+                            w[1] = Lt > 0.f ? 1.f / Lt : 0.f;
+                            if (a.lse != nullptr)
+                                a.lse[qh0 + tid] = Lt > 0.f ? (M + log2f(Lt)) * 0.6931471805599453f
+                                                            : -CUDART_INF_F;
+                        }
+                        if (!group_sync()) {
+                            hs::set_status(a.status, HS_ERR_TIMEOUT);
+                            B.abort = 1;
+                        }
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float o[HG];
@@ -480,6 +527,20 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                             for (int h = 0; h < HG; ++h) o[h] = 0.f;
                         }
                         const int d = c * 128 + tid;
+                        if (cp > 0) {
+#pragma unroll
+                            for (int h = 0; h < HG; ++h) {
+                                const int64_t base = (qh0 + h) * a.part_stride;
+                                const float* w = B.cw[h];
+                                float acc = w[0] * o[h];
+#pragma unroll
+                                for (int pp = 0; pp < kMaxCombine; ++pp)
+                                    if (pp < cp && w[2 + pp] != 0.f)
+                                        acc = fmaf(w[2 + pp], a.part_o[(base + pp) * 512 + d], acc);
+                                a.out[(qh0 + h) * 512 + d] = __float2bfloat16_rn(acc * w[1]);
+                            }
+                            continue;
+                        }
 #pragma unroll
                         for (int h = 0; h < HG; ++h) {
                             const int64_t qh = qh0 + h;
@@ -492,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                             }
                         }
                     }
-                    if (tid < HG) {
+                    if (tid < HG && cp == 0) {
                         float Lh = 0.f, Mh = -CUDART_INF_F;
 #pragma unroll
                         for (int h = 0; h < HG; ++h)

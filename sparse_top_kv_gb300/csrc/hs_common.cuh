@@ -124,6 +124,19 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 16-byte global -> shared copy, completion tracked by cp.async groups or
+// cp.async.mbarrier.arrive.
+__device__ __forceinline__ void tc_cp_async16(uint32_t dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once this thread's cp.async copies issued so far complete
+// (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void tc_cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

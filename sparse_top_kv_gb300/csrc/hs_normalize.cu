@@ -43,13 +43,29 @@ struct NormArgs {
     int32_t* out_count;
     int32_t* err_counts;
     int32_t stage_table;  // 1: the request's block-table row is staged in shared memory
+    int32_t page_shift;   // log2(page_size) when it is a power of two, else -1
 };
+
+// Logical block and in-page offset of position t (0 <= t < 2^31): a shift and
+// a mask for power-of-two pages, 32-bit division otherwise (no 64-bit divide).
+__device__ __forceinline__ void split_pos(int64_t t, const NormArgs& a, int32_t* b, int32_t* off) {
+    const uint32_t ut = uint32_t(t);
+    if (a.page_shift >= 0) {
+        *b = int32_t(ut >> a.page_shift);
+        *off = int32_t(ut & ((1u << a.page_shift) - 1u));
+    } else {
+        const uint32_t ub = ut / uint32_t(a.page_size);
+        *b = int32_t(ub);
+        *off = int32_t(ut - ub * uint32_t(a.page_size));
+    }
+}
 
 // Checks of a position already known to satisfy 0 <= t < T.
 // Returns -1 when valid, else the rejection category (0 range, 2 owner).
 __device__ __forceinline__ int classify_in_range(int64_t t, const int32_t* table,
                                                  const NormArgs& a, int32_t req) {
-    const int64_t b = t / a.page_size;
+    int32_t b, off;
+    split_pos(t, a, &b, &off);
     if (b >= a.max_blocks) return 0;
     const int32_t p = table[b];
     if (p < 0 || p >= a.num_pages) return 0;
@@ -181,9 +197,10 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
                     const int b = __ffs(x) - 1;
                     x &= x - 1;
                     const int64_t t = base + b;
-                    const int64_t p = table[t / a.page_size];
+                    int32_t blk, off;
+                    split_pos(t, a, &blk, &off);
                     otok[pos] = int32_t(t);
-                    oslot[pos] = int32_t(p * a.page_size + t % a.page_size);
+                    oslot[pos] = table[blk] * a.page_size + off;
                     ++pos;
                 }
             }
@@ -224,7 +241,12 @@ extern "C" int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n
     NormArgs a{cand,      rows,      n_cand,     window,    num_sinks, row_req,
                seq_lens,  block_table, bt_stride, max_blocks, page_owner, num_reqs,
                num_pages, page_size, cap,        out_tok,   out_slot,  out_count,
-               err_counts, max_blocks <= kMaxStagedBlocks ? 1 : 0};
+               err_counts, max_blocks <= kMaxStagedBlocks ? 1 : 0, -1};
+    if ((page_size & (page_size - 1)) == 0) {
+        int sh = 0;
+        while ((1 << sh) < page_size) ++sh;
+        a.page_shift = sh;
+    }
     const size_t smem = a.stage_table ? size_t(max_blocks) * sizeof(int32_t) : 0;
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(normalize_kernel),

@@ -10,40 +10,32 @@
 // ring in flight with one issuing thread; contiguous runs become ONE bulk op,
 // per-row ops remain only for scattered rows.
 //
-// GB300 design: a grid of 2-warp CTAs.  Work items are (list, segment of
-// `seg` rows); each CTA derives the item -> list map from the device-side
-// counts (no host round trip) and takes items blockIdx.x, +gridDim.x, ...
-// Warp 0 prefetches the item's indices into shared memory, then its lane 0
-// plans a stage (greedy run detection: consecutive rows whose source and
-// destination both advance by one row are one piece), arms the stage's full
-// mbarrier with the byte count and issues one cp.async.bulk global->shared
-// per piece.  Warp 1 lane 0 waits on the full barrier, issues one
-// cp.async.bulk shared->global per piece, waits until the ring slot has been
-// read, and releases it on the empty barrier.  Every wait is bounded in wall
-// time; a timeout stores HS_ERR_TIMEOUT in the status word, and each role
-// drains its own copies in flight (again bounded) before leaving.
+// GB300 design: every warp works on its own.  Work is cut into groups of up
+// to 32 consecutive rows of one list (as many as fill an 8 KB stage); each
+// CTA derives the group -> list map from the device-side counts (no host
+// round trip) and its warps take groups round-robin over the grid.  A warp
+// keeps a ring of 3 stages in shared memory: a group whose rows are one
+// contiguous run in both source and destination is ONE cp.async.bulk
+// global->shared op armed on the stage's mbarrier with its byte count;
+// scattered rows are fetched with 16-byte cp.async by all 32 lanes (measured
+// on GB300: a per-row bulk op from host memory costs ~0.5 us of the SM's
+// TMA unit, so per-row bulk loads cap a CTA near 2 GB/s, while 16-byte
+// cp.async from all lanes keeps dozens of rows in flight).  A landed stage is
+// written out by the warp's lanes with 16-byte stores (the destinations are
+// scattered slots, and plain stores need no completion tracking), two groups
+// behind the loads so that three stages stay in flight per warp.  The
+// mbarrier waits are bounded in wall time (HS_ERR_TIMEOUT on expiry).
 #include "hs_common.cuh"
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr uint32_t kStageBytes = 32768;
-constexpr int kMaxPieces = 64;
-constexpr int kMaxSeg = 64;
-constexpr int kThreads = 64;
-
-struct Piece {
-    int64_t src_byte;
-    int64_t dst_byte;
-    uint32_t smem_off;
-    uint32_t bytes;
-};
-
-struct StageMeta {
-    int32_t npieces;  // -1: end of work
-    int32_t pad[3];
-    Piece p[kMaxPieces];
-};
+// Each warp owns a ring of kWS stages of kStageBytes in shared memory and
+// copies groups of up to kMaxGroup consecutive rows of one list.
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kWS = 3;
+constexpr uint32_t kStageBytes = 8192;
+constexpr int kMaxGroup = 32;
 
 struct XferArgs {
     const uint8_t* src_base;
@@ -59,227 +51,188 @@ struct XferArgs {
     int32_t fixed_count;
     int32_t nlists;
     int32_t list_stride;
-    int32_t seg;
-    int32_t* dgi;  // swap-in revocation target, or nullptr
-    int32_t zero_bad_src;  // 1: a missing source zeroes the destination (SwapIn)
+    int32_t group;          // rows per group (<= kMaxGroup, group * row_bytes <= kStageBytes)
+    int32_t* dgi;           // swap-in revocation target, or nullptr
+    int32_t zero_bad_src;   // 1: a missing source zeroes the destination (SwapIn)
     int32_t hot_size;
     int64_t region_stride;
     int32_t* status;
     uint64_t timeout_ns;
 };
 
-struct Smem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    int32_t abort;
-    int32_t pad;
-    int64_t idx_src[kMaxSeg];
-    int64_t idx_dst[kMaxSeg];
-    StageMeta meta[kStages];
+struct WarpRing {
+    uint64_t full[kWS];
+    int64_t dst[kWS][kMaxGroup];  // destination row of each staged row, -1 = none
 };
 
-constexpr size_t kRingBytes = size_t(kStages) * kStageBytes;
+constexpr size_t kRingBytes = size_t(kWarps) * kWS * kStageBytes;
 
 __device__ __forceinline__ int64_t list_count(const XferArgs& a, int r) {
     const int64_t c = a.counts ? int64_t(a.counts[r]) : int64_t(a.fixed_count);
     return c < 0 ? 0 : (c > a.list_stride ? a.list_stride : c);
 }
 
+// Writes one landed stage out: the warp's lanes copy 16-byte vectors from
+// shared memory to each staged row's destination.
+__device__ __forceinline__ void store_group(const XferArgs& a, const WarpRing& R, int st,
+                                            const unsigned char* stage, int64_t rb, int nv,
+                                            int lane) {
+    for (int k = 0; k < a.group; ++k) {
+        const int64_t d = R.dst[st][k];
+        if (d < 0) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(stage + int64_t(k) * rb);
+        uint4* dst = reinterpret_cast<uint4*>(a.dst_base + d * rb);
+        for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
     extern __shared__ __align__(128) unsigned char dsmem[];
-    // Layout: [ring kStages * kStageBytes][Smem][prefix int32 nlists+1]
-    unsigned char* ring = dsmem;
-    Smem& S = *reinterpret_cast<Smem*>(dsmem + kRingBytes);
-    int32_t* prefix = reinterpret_cast<int32_t*>(dsmem + kRingBytes + sizeof(Smem));
-
+    // Layout: [ring kWarps * kWS * kStageBytes][WarpRing x kWarps][prefix int32 nlists+1]
+    WarpRing* rings = reinterpret_cast<WarpRing*>(dsmem + kRingBytes);
+    int32_t* prefix = reinterpret_cast<int32_t*>(dsmem + kRingBytes + sizeof(WarpRing) * kWarps);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            hs::mbar_init(&S.full[s], 1);
-            hs::mbar_init(&S.empty[s], 1);
-        }
-        S.abort = 0;
+    WarpRing& R = rings[warp];
+    unsigned char* ring = dsmem + size_t(warp) * kWS * kStageBytes;
+    if (lane == 0) {
+        for (int s = 0; s < kWS; ++s) hs::mbar_init(&R.full[s], 32);
         hs::fence_mbar_init();
     }
-    // Items per list -> prefix sums (warp 0).
+    // Groups per list -> prefix sums (warp 0).
     if (warp == 0) {
         int running = 0;
         if (lane == 0) prefix[0] = 0;
         for (int base = 0; base < a.nlists; base += 32) {
             const int r = base + lane;
-            const int items = r < a.nlists ? int((list_count(a, r) + a.seg - 1) / a.seg) : 0;
-            const int incl = hs::warp_incl_scan(items);
+            const int g = r < a.nlists ? int((list_count(a, r) + a.group - 1) / a.group) : 0;
+            const int incl = hs::warp_incl_scan(g);
             if (r < a.nlists) prefix[r + 1] = running + incl;
             running += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
     __syncthreads();
-    const int total_items = prefix[a.nlists];
+    const int total = prefix[a.nlists];
     const int64_t rb = a.row_bytes;
-    volatile int* abort_flag = &S.abort;
-
-    if (warp == 0) {
-        // ------------------------------ loader ------------------------------
-        int stage = 0;
-        uint32_t ring_par = 0;  // flips each time the ring wraps
-        bool pending[kStages];
-        uint32_t pend_par[kStages];
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) pending[s] = false, pend_par[s] = 0;
-        int ok = 1;
-        for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
-            // List of this item: the last r with prefix[r] <= item.
+    const int nv = int(rb / 16);
+    const int gw = blockIdx.x * kWarps + warp;   // global warp id
+    const int nw = gridDim.x * kWarps;
+    const int mine = gw < total ? (total - gw + nw - 1) / nw : 0;  // groups of this warp
+    bool ok = true;
+    bool bad = false;
+    for (int j = 0; j < mine + kWS - 1 && ok; ++j) {
+        // (a) Issue group j into stage j % kWS.
+        if (j < mine) {
+            const int st = j % kWS;
+            unsigned char* stage = ring + size_t(st) * kStageBytes;
+            const int gidx = gw + j * nw;
             int lo = 0, hi = a.nlists;
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (prefix[mid] <= item) lo = mid; else hi = mid;
+                if (prefix[mid] <= gidx) lo = mid; else hi = mid;
             }
             const int r = lo;
-            const int64_t m0 = int64_t(item - prefix[r]) * a.seg;
-            const int nrows = int(hs::min64(list_count(a, r), m0 + a.seg) - m0);
-            // Index prefetch into shared memory (whole warp, coalesced).
+            const int64_t m0 = int64_t(gidx - prefix[r]) * a.group;
+            const int nrows = int(hs::min64(list_count(a, r), m0 + a.group) - m0);
             const int64_t off = int64_t(r) * a.list_stride + m0;
-            for (int k = lane; k < nrows; k += 32) {
-                S.idx_src[k] = a.src32 ? int64_t(a.src32[off + k]) : a.src64[off + k];
-                S.idx_dst[k] = a.dst32 ? int64_t(a.dst32[off + k]) : a.dst64[off + k];
+            int64_t g = -1, d = -1;
+            if (lane < nrows) {
+                g = a.src32 ? int64_t(a.src32[off + lane]) : a.src64[off + lane];
+                d = a.dst32 ? int64_t(a.dst32[off + lane]) : a.dst64[off + lane];
             }
+            const bool src_ok = g >= 0 && (a.src_limit < 0 || g < a.src_limit);
+            const bool dst_ok = d >= 0 && (a.dst_limit < 0 || d < a.dst_limit);
+            bool copy = lane < nrows && src_ok && dst_ok;
+            if (lane < nrows && !dst_ok) bad = true;
+            if (lane < nrows && dst_ok && !src_ok && (!a.zero_bad_src || a.dgi == nullptr))
+                bad = true;
+            // Rows without a source: zero the destination and revoke the slot.
+            unsigned zmask = __ballot_sync(0xffffffffu, lane < nrows && dst_ok && !src_ok &&
+                                                           a.zero_bad_src);
+            while (zmask) {
+                const int k = __ffs(zmask) - 1;
+                zmask &= zmask - 1;
+                const int64_t dk = __shfl_sync(0xffffffffu, d, k);
+                uint4* z = reinterpret_cast<uint4*>(a.dst_base + dk * rb);
+                for (int v = lane; v < nv; v += 32) z[v] = make_uint4(0, 0, 0, 0);
+                if (lane == 0 && a.dgi != nullptr) {
+                    const int64_t s = dk - int64_t(r) * a.region_stride;
+                    if (s >= 0 && s < a.hot_size) a.dgi[int64_t(r) * a.hot_size + s] = -1;
+                }
+            }
+            // The stage's previous group was written out (synchronously) at
+            // an earlier iteration by every lane of this warp.
             __syncwarp();
-            if (lane == 0) {
-                int k = 0;
-                while (k < nrows) {
-                    if (!hs::mbar_wait_bounded(&S.empty[stage], ring_par ^ 1u, a.timeout_ns,
-                                               abort_flag)) {
-                        ok = 0;
-                        break;
-                    }
-                    pending[stage] = false;
-                    StageMeta& M = S.meta[stage];
-                    int np = 0;
-                    uint32_t used = 0;
-                    while (k < nrows && np < kMaxPieces) {
-                        const int64_t g = S.idx_src[k];
-                        const int64_t d = S.idx_dst[k];
-                        const bool src_ok = g >= 0 && (a.src_limit < 0 || g < a.src_limit);
-                        const bool dst_ok = d >= 0 && (a.dst_limit < 0 || d < a.dst_limit);
-                        if (!dst_ok) {  // nothing may be written there
-                            hs::set_status(a.status, HS_ERR_BAD_INDEX);
-                            ++k;
-                            continue;
-                        }
-                        if (!src_ok && !a.zero_bad_src) {
-                            hs::set_status(a.status, HS_ERR_BAD_INDEX);
-                            ++k;
-                            continue;
-                        }
-                        if (!src_ok) {
-                            // No source row: zero the destination and revoke the slot.
-                            uint4* z = reinterpret_cast<uint4*>(a.dst_base + d * rb);
-                            for (int64_t v = 0; v < rb / 16; ++v) z[v] = make_uint4(0, 0, 0, 0);
-                            if (a.dgi != nullptr) {
-                                const int64_t s = d - int64_t(r) * a.region_stride;
-                                if (s >= 0 && s < a.hot_size)
-                                    a.dgi[int64_t(r) * a.hot_size + s] = -1;
-                            } else {
-                                hs::set_status(a.status, HS_ERR_BAD_INDEX);
-                            }
-                            ++k;
-                            continue;
-                        }
-                        const int64_t room = (int64_t(kStageBytes) - used) / rb;
-                        if (room <= 0) break;
-                        int64_t run = 1;
-                        while (k + run < nrows && run < room && S.idx_src[k + run] == g + run &&
-                               S.idx_dst[k + run] == d + run &&
-                               (a.src_limit < 0 || g + run < a.src_limit) &&
-                               (a.dst_limit < 0 || d + run < a.dst_limit))
-                            ++run;
-                        M.p[np].src_byte = g * rb;
-                        M.p[np].dst_byte = d * rb;
-                        M.p[np].smem_off = used;
-                        M.p[np].bytes = uint32_t(run * rb);
-                        ++np;
-                        used += uint32_t(run * rb);
-                        k += int(run);
-                    }
-                    M.npieces = np;
-                    unsigned char* buf = ring + size_t(stage) * kStageBytes;
-                    // One arrival (count 1) carrying the byte count, then the copies.
-                    hs::mbar_arrive_expect_tx(&S.full[stage], used);
-                    for (int p = 0; p < np; ++p)
-                        hs::bulk_g2s(buf + M.p[p].smem_off, a.src_base + M.p[p].src_byte,
-                                     M.p[p].bytes, &S.full[stage]);
-                    pending[stage] = true;
-                    pend_par[stage] = ring_par;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ring_par ^= 1u;
-                    }
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        if (lane == 0) {
-            if (ok) {
-                // End-of-work marker for the storer.
-                if (hs::mbar_wait_bounded(&S.empty[stage], ring_par ^ 1u, a.timeout_ns,
-                                          abort_flag)) {
-                    S.meta[stage].npieces = -1;
-                    hs::mbar_arrive(&S.full[stage]);
+            if (lane < kMaxGroup) R.dst[st][lane] = copy ? d : int64_t(-1);
+            const unsigned cmask = __ballot_sync(0xffffffffu, copy);
+            // One contiguous run of valid rows (source and destination) -> one
+            // bulk op; otherwise 16-byte copies by the whole warp.
+            const int64_t g0 = __shfl_sync(0xffffffffu, g, 0);
+            const int64_t d0 = __shfl_sync(0xffffffffu, d, 0);
+            const bool in_run = !(lane < nrows) || (copy && g == g0 + lane && d == d0 + lane);
+            const bool one_run = nrows > 1 && cmask == ((nrows == 32) ? 0xffffffffu : ((1u << nrows) - 1u)) &&
+                                 __all_sync(0xffffffffu, in_run);
+            __syncwarp();
+            if (one_run) {
+                if (lane == 0) {
+                    const uint32_t bytes = uint32_t(nrows * rb);
+                    hs::mbar_arrive_expect_tx(&R.full[st], bytes);
+                    hs::bulk_g2s(stage, a.src_base + g0 * rb, bytes, &R.full[st]);
                 } else {
-                    ok = 0;
+                    hs::mbar_arrive(&R.full[st]);
                 }
-            }
-            if (!ok) {
-                hs::set_status(a.status, HS_ERR_TIMEOUT);
-                S.abort = 1;
-                // Drain the loads this thread issued (bounded).
-                for (int s = 0; s < kStages; ++s)
-                    if (pending[s])
-                        hs::mbar_wait_bounded(&S.full[s], pend_par[s], a.timeout_ns, nullptr);
+            } else {
+                unsigned m = cmask;
+                while (m) {
+                    const int k = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int64_t gk = __shfl_sync(0xffffffffu, g, k);
+                    const unsigned char* src = a.src_base + gk * rb;
+                    const uint32_t dsm = hs::smem_u32(stage + int64_t(k) * rb);
+                    for (int v = lane; v < nv; v += 32)
+                        hs::tc_cp_async16(dsm + v * 16, src + v * 16);
+                }
+                hs::tc_cp_async_arrive_noinc(&R.full[st]);
             }
         }
-    } else if (lane == 0) {
-        // ------------------------------ storer ------------------------------
-        int stage = 0;
-        uint32_t ring_par = 0;
-        for (;;) {
-            if (!hs::mbar_wait_bounded(&S.full[stage], ring_par, a.timeout_ns, abort_flag)) {
-                if (!*abort_flag) hs::set_status(a.status, HS_ERR_TIMEOUT);
-                S.abort = 1;
+        // (b) Store group j - (kWS - 1) once it has landed.
+        const int js = j - (kWS - 1);
+        if (js >= 0 && js < mine) {
+            const int st = js % kWS;
+            const bool landed = hs::mbar_wait_bounded(&R.full[st], (js / kWS) & 1, a.timeout_ns);
+            if (!__all_sync(0xffffffffu, landed)) {
+                ok = false;
                 break;
             }
-            const StageMeta& M = S.meta[stage];
-            const int np = M.npieces;
-            if (np < 0) break;
-            const unsigned char* buf = ring + size_t(stage) * kStageBytes;
-            for (int p = 0; p < np; ++p)
-                hs::bulk_s2g(a.dst_base + M.p[p].dst_byte, buf + M.p[p].smem_off, M.p[p].bytes);
-            hs::bulk_commit();
-            hs::bulk_wait_read_all();
-            hs::mbar_arrive(&S.empty[stage]);
-            if (++stage == kStages) {
-                stage = 0;
-                ring_par ^= 1u;
-            }
+            __syncwarp();
+            store_group(a, R, st, ring + size_t(st) * kStageBytes, rb, nv, lane);
+            __syncwarp();
         }
-        hs::bulk_wait_all();
     }
+    if (!ok) hs::set_status(a.status, HS_ERR_TIMEOUT);
+    if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+    // Leave no copy into shared memory in flight (bounded: the waits above
+    // only give up after the wall-time limit).
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 size_t xfer_smem_bytes(int nlists) {
-    return kRingBytes + sizeof(Smem) + sizeof(int32_t) * (size_t(nlists) + 1);
+    return kRingBytes + sizeof(WarpRing) * kWarps + sizeof(int32_t) * (size_t(nlists) + 1);
 }
 
 constexpr int kMaxSmem = 227 * 1024;
 
-int launch_xfer(const XferArgs& a, int64_t max_items, hs_stream_t stream) {
+int launch_xfer(XferArgs a, int64_t max_items_rows, int max_ctas, hs_stream_t stream) {
     const size_t smem = xfer_smem_bytes(a.nlists);
     if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(xfer_kernel), smem,
                                                 smem_set);
     if (rc != HS_OK) return rc;
-    const int64_t grid = hs::max64(1, hs::min64(max_items, hs_host::num_sms()));
+    a.group = int32_t(hs::max64(1, hs::min64(kMaxGroup, int64_t(kStageBytes) / a.row_bytes)));
+    const int64_t groups = (max_items_rows + a.group - 1) / a.group;
+    // Two CTAs (96 KB of stages each) fit one SM.
+    const int64_t budget = max_ctas > 0 ? max_ctas : 2 * int64_t(hs_host::num_sms());
+    const int64_t grid = hs::max64(1, hs::min64((groups + kWarps - 1) / kWarps, budget));
     xfer_kernel<<<int(grid), kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();
 }
@@ -291,9 +244,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, int64_t row_bytes,
                           const int32_t* miss_src, const int64_t* miss_dst,
                           const int32_t* miss_count, int32_t rows, int32_t cap, int32_t* dgi,
-                          int32_t hot_size, int64_t region_stride, int32_t* status,
-                          hs_stream_t stream) {
-    if (rows < 0 || cap < 0 || host_rows < 0 || row_bytes <= 0) return HS_ERR_INVALID_ARG;
+                          int32_t hot_size, int64_t region_stride, int32_t max_ctas,
+                          int32_t* status, hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || host_rows < 0 || row_bytes <= 0 || max_ctas < 0)
+        return HS_ERR_INVALID_ARG;
     if (row_bytes % 16 != 0) return HS_ERR_MISALIGNED;
     if (row_bytes > int64_t(kStageBytes)) return HS_ERR_CAPACITY;
     if (rows == 0 || cap == 0) return HS_OK;
@@ -313,15 +267,13 @@ extern "C" int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, i
     a.counts = miss_count;
     a.nlists = rows;
     a.list_stride = cap;
-    a.seg = kMaxSeg;
     a.dgi = dgi;
     a.zero_bad_src = 1;
     a.hot_size = hot_size;
     a.region_stride = region_stride;
     a.status = status;
     a.timeout_ns = hs::kWaitTimeoutNs;
-    const int64_t max_items = int64_t(rows) * ((cap + kMaxSeg - 1) / kMaxSeg);
-    return launch_xfer(a, max_items, stream);
+    return launch_xfer(a, int64_t(rows) * cap, max_ctas, stream);
 }
 
 extern "C" int hs_backup(const void* src, const int64_t* src_rows, void* host_pool,
@@ -334,7 +286,6 @@ extern "C" int hs_backup(const void* src, const int64_t* src_rows, void* host_po
     if (src == nullptr || src_rows == nullptr || host_pool == nullptr || dst_slots == nullptr)
         return HS_ERR_INVALID_ARG;
     if (!aligned16(src) || !aligned16(host_pool)) return HS_ERR_MISALIGNED;
-    constexpr int kBackupSeg = 8;
     XferArgs a{};
     a.src_base = static_cast<const uint8_t*>(src);
     a.dst_base = static_cast<uint8_t*>(host_pool);
@@ -347,8 +298,7 @@ extern "C" int hs_backup(const void* src, const int64_t* src_rows, void* host_po
     a.fixed_count = n;
     a.nlists = 1;
     a.list_stride = n;
-    a.seg = kBackupSeg;
     a.status = status;
     a.timeout_ns = hs::kWaitTimeoutNs;
-    return launch_xfer(a, (int64_t(n) + kBackupSeg - 1) / kBackupSeg, stream);
+    return launch_xfer(a, n, 0, stream);
 }

@@ -38,7 +38,7 @@ _SIGS = {
     "hs_hot_state_reset": ([_P, _P, _I32, _I32, _P], ctypes.c_int),
     "hs_hot_lookup_assign": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
                               _P, _P, _P, _P, _P, _P], ctypes.c_int),
-    "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _P, _P],
+    "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _I32, _P, _P],
                    ctypes.c_int),
     "hs_backup": ([_P, _P, _P, _P, _I32, _I64, _I64, _P, _P], ctypes.c_int),
     "hs_sparse_decode_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32], _I64),
@@ -49,6 +49,9 @@ _SIGS = {
     "hs_sparse_decode_partial": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
                                   _I32, _I32, _F32, _P, _P, _P, _I32, _I32, _P, _P],
                                  ctypes.c_int),
+    "hs_sparse_decode_finish": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
+                                 _I32, _I32, _F32, _P, _P, _P, _I32, _I32, _P, _P, _P, _P],
+                                ctypes.c_int),
     "hs_sparse_decode_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
                                   _I32, _I32, _F32, _P, _P, _P, _P], ctypes.c_int),
 }
@@ -184,7 +187,7 @@ def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, 
 
 
 def swap_in(host_pool_dev, host_rows, hot, row_bytes, miss_src, miss_dst, miss_count, *,
-            dgi=None, hot_size=0, region_stride=0, status=None, stream=None):
+            dgi=None, hot_size=0, region_stride=0, max_ctas=0, status=None, stream=None):
     """S3 SwapIn.  host_pool_dev: device-visible address (int) of the pinned pool."""
     _check(miss_src, torch.int32, "miss_src")
     _check(miss_dst, torch.int64, "miss_dst")
@@ -194,7 +197,7 @@ def swap_in(host_pool_dev, host_rows, hot, row_bytes, miss_src, miss_dst, miss_c
     rows, cap = miss_src.shape
     _call("hs_swap_in", ctypes.c_void_p(host_pool_dev), host_rows, _ptr(hot), row_bytes,
           _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), rows, cap, _ptr(dgi), hot_size,
-          region_stride, _ptr(status), _stream(stream))
+          region_stride, max_ctas, _ptr(status), _stream(stream))
 
 
 def backup(src, src_rows, host_pool_dev, dst_slots, row_bytes, host_rows, *, status=None,
@@ -261,6 +264,30 @@ def sparse_decode_partial(q, k_base, v_base, row_stride, kv_head_stride, num_kv_
           d_qk, d_v, float(scale), _ptr(part_m), _ptr(part_l), _ptr(part_o), parts, part_base,
           _ptr(status), _stream(stream))
     return sparse_decode_partial_splits(rows, heads, kv_heads, cap, d_qk, d_v)
+
+
+def sparse_decode_finish(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows,
+                         count, scale, d_v, part_m, part_l, part_o, parts_used, *, out=None,
+                         lse=None, status=None, stream=None):
+    """Attend over kv_rows, merge with partial columns [0, parts_used) and
+    write the final (out bf16 [rows, heads, d_v], lse fp32 [rows, heads])."""
+    _check(q, torch.bfloat16, "q")
+    _check(kv_rows, torch.int32, "kv_rows")
+    _check(count, torch.int32, "count")
+    for t, n in ((part_m, "part_m"), (part_l, "part_l"), (part_o, "part_o")):
+        _check(t, torch.float32, n)
+    _check(status, torch.int32, "status")
+    rows, heads, d_qk = q.shape
+    _, kv_heads, cap = kv_rows.shape
+    if out is None:
+        out = torch.empty(rows, heads, d_v, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=q.device)
+    _call("hs_sparse_decode_finish", _ptr(q), _ptr(k_base), _ptr(v_base), row_stride,
+          kv_head_stride, num_kv_rows, _ptr(kv_rows), _ptr(count), rows, cap, heads, kv_heads,
+          d_qk, d_v, float(scale), _ptr(part_m), _ptr(part_l), _ptr(part_o), part_m.shape[-1],
+          parts_used, _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    return out, lse
 
 
 def merge_states(m, l, o, *, out=None, lse=None, stream=None):

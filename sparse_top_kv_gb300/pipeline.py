@@ -72,8 +72,15 @@ class HiSparseDecoder:
         self.part_l = torch.empty(R * heads, P, **f32)
         self.part_o = torch.empty(R * heads, P, d_v, **f32)
         self.side = torch.cuda.Stream(device=dev)
+        self.ev_newrow = torch.cuda.Event()
         self.ev_lists = torch.cuda.Event()
         self.ev_swapped = torch.cuda.Event()
+        # SMs left to the SwapIn while the resident-row attention runs (one
+        # attention CTA per SM; two copy CTAs fit one SM).
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        hg = 64 if heads % 64 == 0 else (32 if heads % 32 == 0 else 16)
+        attn_ctas = R * max(1, heads // hg) * max(1, self.parts_hit)
+        self.swap_ctas = max(32, 2 * (sms - attn_ctas))
 
     def warm_pool(self, page_bytes=65536):
         """One-time set-up pass: read one row of every `page_bytes` of the host
@@ -114,8 +121,9 @@ class HiSparseDecoder:
         attention over the swapped rows (miss_rows) follows the SwapIn, and the
         two sets of partial states are merged with eq. (7).
         `events`, if given, is a list of 7 CUDA events recorded before S1, after
-        S1, after S2, after SwapIn (side), after BackUp (side), after the
-        resident-row attention and at the end of the step."""
+        S1, after S2, after SwapIn (side; BackUp runs first on that stream, in
+        the shadow of S1/S2), again after SwapIn, after the resident-row
+        attention and at the end of the step."""
         R = self.num_reqs
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side
@@ -124,6 +132,11 @@ class HiSparseDecoder:
         with torch.cuda.stream(main):
             self.hot.index_copy_(0, self.reserved_rows, new_row)
         rec(0, main)
+        self.ev_newrow.record(main)
+        # Side stream: host link traffic.  BackUp needs only the new row.
+        side.wait_event(self.ev_newrow)
+        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
+                  self.host_rows, status=self.status, stream=side)
         tok, slot, count, err = hs.normalize_indices(
             cand, self.row_req, seq_lens, self.block_table, self.page_size,
             window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
@@ -135,14 +148,12 @@ class HiSparseDecoder:
                                            stream=main)
         rec(2, main)
         self.ev_lists.record(main)
-        # Side stream: host link traffic.
         side.wait_event(self.ev_lists)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
-                   region_stride=self.region_stride, status=self.status, stream=side)
+                   region_stride=self.region_stride, max_ctas=self.swap_ctas,
+                   status=self.status, stream=side)
         rec(3, side)
-        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
-                  self.host_rows, status=self.status, stream=side)
         rec(4, side)
         self.ev_swapped.record(side)
         # Main stream: HBM traffic over the resident rows meanwhile.
@@ -154,13 +165,47 @@ class HiSparseDecoder:
                                  status=self.status, stream=main)
         rec(5, main)
         main.wait_event(self.ev_swapped)
-        hs.sparse_decode_partial(qv, self.hot, self.hot, self.row_width, 0, nkv,
-                                 miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),
-                                 self.scale, self.d_v, self.part_m, self.part_l, self.part_o,
-                                 self.parts_hit, status=self.status, stream=main)
-        hs.merge_states(self.part_m, self.part_l, self.part_o, out=self.out.view(R * self.heads, -1),
-                        lse=self.lse.view(-1), stream=main)
+        # The swapped rows, merged with the resident-row states (eq. 7).
+        hs.sparse_decode_finish(qv, self.hot, self.hot, self.row_width, 0, nkv,
+                                miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),
+                                self.scale, self.d_v, self.part_m, self.part_l, self.part_o,
+                                self.parts_hit, out=self.out, lse=self.lse, status=self.status,
+                                stream=main)
         rec(6, main)
+        return self.out, self.lse
+
+    def capture(self, events=None):
+        """Capture one decode step over static input buffers (`self.graph_in`)
+        as a CUDA graph, both streams included.  `replay(...)` then copies a
+        step's inputs into those buffers and runs the step with one graph
+        launch.  Run at least one eager step first (it performs the one-time
+        library set-up that capture must not do).  `events`, if given, are
+        timing events recorded inside the graph (see `step`)."""
+        R, dev = self.num_reqs, self.device
+        self.graph_in = dict(
+            cand=torch.empty(R, self.top_k, dtype=torch.int32, device=dev),
+            seq=torch.empty(R, dtype=torch.int32, device=dev),
+            newest=torch.empty(R, dtype=torch.int32, device=dev),
+            new_row=torch.empty(R, self.row_width, dtype=self.hot.dtype, device=dev),
+            q=torch.empty(R, self.heads, self.d_qk, dtype=torch.bfloat16, device=dev))
+        gi = self.graph_in
+        g = torch.cuda.CUDAGraph()
+        self.side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(g):
+            self.step(gi["cand"], gi["seq"], gi["newest"], gi["new_row"], gi["q"],
+                      events=events)
+        self.graph = g
+        return g
+
+    def replay(self, cand, seq_lens, newest_slot, new_row, q):
+        """One decode step through the captured graph (see `capture`)."""
+        gi = self.graph_in
+        gi["cand"].copy_(cand, non_blocking=True)
+        gi["seq"].copy_(seq_lens, non_blocking=True)
+        gi["newest"].copy_(newest_slot, non_blocking=True)
+        gi["new_row"].copy_(new_row, non_blocking=True)
+        gi["q"].copy_(q, non_blocking=True)
+        self.graph.replay()
         return self.out, self.lse
 
     @staticmethod
@@ -168,6 +213,7 @@ class HiSparseDecoder:
         return q if q.dtype == torch.bfloat16 else q.view(torch.bfloat16)
 
     # Kernels of libhs launched by one step (index_copy_ above is torch's):
-    # S1, S2, SwapIn, BackUp, two attention passes, merge.
+    # BackUp, S1, S2, SwapIn, resident-row attention, swapped-row attention
+    # with the merge in its epilogue.
     def launches_per_step(self):
-        return 7
+        return 6

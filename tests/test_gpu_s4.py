@@ -153,6 +153,9 @@ def test_partial_passes_merge_to_the_full_set(heads, d):
     hs.sparse_decode_partial(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb), 1 / math.sqrt(d), d_v,
                              pm, pl, po, pa, status=status)
     out, lse = hs.merge_states(pm, pl, po)  # the extra empty column (l = 0) is skipped
+    # The fused last pass: the second half attended and merged in one call.
+    out2, lse2 = hs.sparse_decode_finish(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb),
+                                         1 / math.sqrt(d), d_v, pm, pl, po, pa, status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
     sample = [0, 7, rows - 1]
@@ -162,6 +165,7 @@ def test_partial_passes_merge_to_the_full_set(heads, d):
                                             count[sample], 1 / math.sqrt(d), d_v=d_v)
     idx = torch.tensor(sample, device="cuda")
     check_attention(out.view(rows, H, d_v)[idx], lse.view(rows, H)[idx], ref_out, ref_lse)
+    check_attention(out2[idx], lse2[idx], ref_out, ref_lse, label="finish")
 
 
 def test_merge_states_kernel():
