@@ -26,7 +26,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from sparse_top_kv_gb300 import hs, inputs  # noqa: E402
+from sparse_top_kv_gb300 import hs, inputs, replicas  # noqa: E402
 from sparse_top_kv_gb300.pipeline import HiSparseDecoder  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
@@ -109,10 +109,8 @@ def ev():
 # ----------------------------------------------------------------------------
 def setup_full(steps, rank):
     cfg = inputs.full_hisparse(steps=steps)
-    if rank:
-        # Weak scaling: every rank serves its own batch of requests.
-        rng = np.random.default_rng(1000 + rank)
-        cfg["block_table"] = cfg["block_table"][rng.permutation(cfg["num_reqs"])]
+    # Weak scaling: every rank serves its own batch of requests.
+    cfg["block_table"] = cfg["block_table"][replicas.rank_request_order(cfg["num_reqs"], rank)]
     return cfg
 
 
@@ -199,10 +197,7 @@ def run_full(args, rank, world, flush):
     clk = clocks.stop()
     swap_bytes = miss_total * ROW_BYTES
     assert int(dec.status.item()) == 0, f"device status {dec.status.item()}"
-    t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = replicas.max_over_ranks(total_ms)
     K = args.steps
     res = dict(total_ms=total_ms, K=K, stage_ms=(stage_ms / K).tolist(),
                hit_rate=hit_total / max(1, hit_total + miss_total),
@@ -248,7 +243,7 @@ def run_e2e(args, cfg, flush):
         e1.synchronize()
         if s >= args.warmup:
             total += e0.elapsed_time(e1)
-    return dict(total_ms=total, h2d=h2d, d2h=d2h)
+    return dict(total_ms=replicas.max_over_ranks(total), h2d=h2d, d2h=d2h)
 
 
 # ----------------------------------------------------------------------------
@@ -401,6 +396,90 @@ def bench_gqa(hbm_peak, flush, reps=20):
             "s4_bytes": nbytes, "s4_gbs": nbytes / t / 1e6, "hbm_frac": nbytes / t / 1e6 / hbm_peak}
 
 
+def h2d_ceiling(pool, nbytes, reps=5):
+    """The host-link ceiling measured in this run: one pinned cudaMemcpyAsync
+    host -> device of `nbytes` from the pool (median of `reps`), GB/s."""
+    nbytes = min(nbytes, pool.numel() * pool.element_size())
+    src = pool.view(torch.uint8).view(-1)[:nbytes]
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    t = []
+    for i in range(reps + 2):
+        a, b = ev(), ev()
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if i >= 2:
+            t.append(a.elapsed_time(b))
+    del dst
+    return nbytes / statistics.median(t) / 1e6
+
+
+# ----------------------------------------------------------------------------
+def profile_run(workload):
+    """For profilers (ncu --profile-from-start off): set the workload up, run
+    it a few times, then run it once more between cudaProfilerStart/Stop.
+    Prints nothing; times nothing."""
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    if workload == "full_hisparse":
+        S = 6
+        cfg = setup_full(S, 0)
+        dec = make_decoder(cfg)
+        dec.warm_pool()
+        di = device_inputs(cfg, dec)
+        for s in range(S):
+            flush_l2(flush)
+            torch.cuda.synchronize()
+            if s == S - 1:
+                torch.cuda.profiler.start()
+            dec.step(di["cand"][s], di["seq"][s], di["newest"][s], di["new_rows"][s], di["q"][s])
+            torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        assert int(dec.status.item()) == 0
+        return
+    if workload == "mla_decode":
+        cfg = inputs.mla_decode()
+        R, H, d_qk, d_v = cfg["num_reqs"], cfg["heads"], 576, 512
+        page, q, k, v, row_stride, head_stride = 64, cfg["q"], cfg["cache"], cfg["cache"], 576, 0
+        extra = {}
+    elif workload == "gqa_union":
+        cfg = inputs.gqa_union()
+        R, H, d_qk = cfg["num_reqs"], cfg["heads"], cfg["d"]
+        d_v, page, q = d_qk, 16, cfg["q"]
+        k, v = cfg["k_cache"], cfg["v_cache"]
+        row_stride, head_stride = cfg["kv_heads"] * d_qk, d_qk
+        extra = dict(window=256, num_sinks=4)
+    else:
+        raise SystemExit(f"unknown workload {workload}")
+    G = cfg.get("kv_heads", 1)
+    cand = torch.from_numpy(cfg["cand"]).cuda()
+    row_req = (torch.from_numpy(cfg["row_req"]).cuda() if "row_req" in cfg
+               else torch.arange(R, dtype=torch.int32, device="cuda"))
+    seq = torch.full((R,), cfg["ctx"], dtype=torch.int32, device="cuda")
+    bt = torch.from_numpy(cfg["block_table"]).cuda()
+    out1 = hs.normalize_indices(cand, row_req, seq, bt, page, num_pages=cfg["num_pages"], **extra)
+    tok, slot, count, err = out1
+    cap = slot.shape[1]
+    out = torch.empty(R, H, d_v, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(R, H, dtype=torch.float32, device="cuda")
+    ws = hs.sparse_decode_workspace_bytes(R, H, G, cap, d_qk, d_v)
+    wsb = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for i in range(4):
+        flush_l2(flush)
+        torch.cuda.synchronize()
+        if i == 3:
+            torch.cuda.profiler.start()
+        hs.normalize_indices(cand, row_req, seq, bt, page, num_pages=cfg["num_pages"], out=out1,
+                             **extra)
+        hs.sparse_decode(q, k, v, row_stride, head_stride, k.shape[0], slot.view(R, G, cap),
+                         count.view(R, G), cfg["scale"], d_v, out=out, lse=lse, workspace=wsb,
+                         status=status)
+        torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    assert status.item() == 0
+
+
 # ----------------------------------------------------------------------------
 def oracle_steps(cfg, steps, attend_rows):
     """Time the oracle's decode step (S1-S3 + BackUp on every request, S4 on
@@ -461,7 +540,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--profile", default=None,
+                    choices=["full_hisparse", "mla_decode", "gqa_union"],
+                    help="run one workload once inside cudaProfilerStart/Stop and exit "
+                         "(for ncu --profile-from-start off); prints no JSON")
     args = ap.parse_args()
+    if args.profile:
+        hs.lib()
+        profile_run(args.profile)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -481,9 +568,9 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     full = run_full(args, rank, world, flush)
     K = full["K"]
-    value = world * K / (full["total_ms"] / 1e3)
+    value = replicas.whole_job_throughput(K, world, full["total_ms"])
     e2e = run_e2e(args, full["cfg"], flush)
-    e2e_value = K / (e2e["total_ms"] / 1e3) * world
+    e2e_value = replicas.whole_job_throughput(K, world, e2e["total_ms"])
     stage = full["stage_ms"]
     # Roofline of the dominant kernel of the step: the resident-row attention
     # pass (HBM) runs concurrently with the SwapIn (host link).
@@ -501,14 +588,16 @@ def main():
     if world == 1 and not args.no_extras:
         extras["swapin"] = bench_swapin()
         torch.cuda.empty_cache()
-    ceiling = extras.get("swapin", {}).get("ceiling_gbs")
+    # Host-link ceiling in this run: pinned H2D memcpy of 302 MB (the size of
+    # the swapin workload's copy) from this workload's own pool.
+    ceiling = h2d_ceiling(full["cfg"]["pool"], 64 * 4096 * ROW_BYTES)
     swap_gbs = full["swap_bytes_per_step"] / swap_ms / 1e6 if swap_ms > 0 else 0.0
     roof_swap = {"kernel": "hs_swap_in", "bound": "host_link", "achieved": swap_gbs,
                  "peak": ceiling, "unit": "GB/s",
                  "frac": (swap_gbs / ceiling) if ceiling else None,
                  "traffic": NCU_TRAFFIC["swap_in"],
                  "bytes_per_launch": full["swap_bytes_per_step"],
-                 "peak_source": "in-run pinned cudaMemcpyAsync H2D of 302 MB"}
+                 "peak_source": "in-run pinned cudaMemcpyAsync H2D of 302 MB from the pool"}
     dominant = roof_attn if attn_ms >= swap_ms else roof_swap
     if world == 1 and not args.no_extras:
         extras["mla_decode"] = bench_mla_decode(hbm_peak, flush)
@@ -566,10 +655,10 @@ def run_reference(args, rank, world):
         return
     S = args.warmup + args.steps
     cfg = inputs.full_hisparse(steps=S)
-    from oracle.pipeline import OracleHiSparse  # noqa: F401
+    # Both passes start from a cold oracle state over the same pool: BackUp
+    # writes the same rows in both, and step s reads only positions < T_s.
     t_s4 = oracle_steps(cfg, S, attend_rows=[0, 1, 2, 3])
-    cfg2 = inputs.full_hisparse(steps=S)
-    t_nos4 = oracle_steps(cfg2, S, attend_rows=[])
+    t_nos4 = oracle_steps(cfg, S, attend_rows=[])
     per = [b + max(0.0, a - b) * 16 for a, b in zip(t_s4, t_nos4)]
     timed = per[args.warmup:]
     total = sum(timed)
