@@ -52,7 +52,8 @@ int ensure_dynamic_smem(const void* func, size_t bytes, int* cache) {
         cudaSuccess)
         return HS_ERR_CUDA;
     if (bytes + fa.sharedSizeBytes > size_t(optin)) return HS_ERR_CAPACITY;
-    if (bytes > 48 * 1024 &&
+    // Without the opt-in, static + dynamic shared memory must fit 48 KB.
+    if (bytes + fa.sharedSizeBytes > 48 * 1024 &&
         cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) !=
             cudaSuccess)
         return HS_ERR_CUDA;

@@ -76,6 +76,7 @@ __device__ __forceinline__ int classify_in_range(int64_t t, const int32_t* table
 __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
     extern __shared__ int32_t s_table[];  // [max_blocks] when a.stage_table
     __shared__ uint32_t bm[kWindowWords];
+    __shared__ int wpos[kWindowWords];  // output offset of each bitmap word
     __shared__ int scan_scratch[33];
     __shared__ int s_err[4];
 
@@ -178,9 +179,14 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
             if (ed) atomicAdd(&s_err[3], ed);
             __syncthreads();
 
-            // Ascending compaction of the window.
-            uint32_t words[kWordsPerThread];
+            // Ascending compaction of the window: the output offset of every
+            // word from one block scan (thread tid counts words 8 tid ..
+            // 8 tid + 7), then the words are emitted round-robin (word w by
+            // thread w mod 512), so a dense run of positions -- recent tokens
+            // under a recency-skewed selection -- is spread over consecutive
+            // threads instead of falling on one.
             int cnt = 0;
+            uint32_t words[kWordsPerThread];
 #pragma unroll
             for (int k = 0; k < kWordsPerThread; ++k) {
                 const int w = tid * kWordsPerThread + k;
@@ -188,11 +194,17 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
                 cnt += __popc(words[k]);
             }
             int total;
-            int pos = out_n + hs::block_excl_scan(cnt, scan_scratch, &total);
+            int run = out_n + hs::block_excl_scan(cnt, scan_scratch, &total);
 #pragma unroll
             for (int k = 0; k < kWordsPerThread; ++k) {
-                uint32_t x = words[k];
-                const int64_t base = lo + int64_t(tid * kWordsPerThread + k) * 32;
+                wpos[tid * kWordsPerThread + k] = run;
+                run += __popc(words[k]);
+            }
+            __syncthreads();
+            for (int w = tid; w < nw; w += kThreads) {
+                uint32_t x = bm[w];
+                int pos = wpos[w];
+                const int64_t base = lo + int64_t(w) * 32;
                 while (x) {
                     const int b = __ffs(x) - 1;
                     x &= x - 1;

@@ -121,9 +121,8 @@ class HiSparseDecoder:
         attention over the swapped rows (miss_rows) follows the SwapIn, and the
         two sets of partial states are merged with eq. (7).
         `events`, if given, is a list of 7 CUDA events recorded before S1, after
-        S1, after S2, after SwapIn (side; BackUp runs first on that stream, in
-        the shadow of S1/S2), again after SwapIn, after the resident-row
-        attention and at the end of the step."""
+        S1, after S2, after BackUp + SwapIn (side stream), again after them,
+        after the resident-row attention and at the end of the step."""
         R = self.num_reqs
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side
@@ -132,11 +131,6 @@ class HiSparseDecoder:
         with torch.cuda.stream(main):
             self.hot.index_copy_(0, self.reserved_rows, new_row)
         rec(0, main)
-        self.ev_newrow.record(main)
-        # Side stream: host link traffic.  BackUp needs only the new row.
-        side.wait_event(self.ev_newrow)
-        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
-                  self.host_rows, status=self.status, stream=side)
         tok, slot, count, err = hs.normalize_indices(
             cand, self.row_req, seq_lens, self.block_table, self.page_size,
             window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
@@ -148,7 +142,12 @@ class HiSparseDecoder:
                                            stream=main)
         rec(2, main)
         self.ev_lists.record(main)
+        # Side stream: host-link traffic, after S2 (a copy to host memory that
+        # shares an SM with S1 or S2 stalls them).  BackUp needs only the new
+        # rows, written before S1.
         side.wait_event(self.ev_lists)
+        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
+                  self.host_rows, status=self.status, stream=side)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
                    region_stride=self.region_stride, max_ctas=self.swap_ctas,
