@@ -209,7 +209,11 @@ int hs_backup(const void* src, const int64_t* src_rows, void* host_pool,
  *            round to nearest even).
  * lse        fp32 [rows, heads] natural-log LSE, or NULL.
  * workspace  device scratch of at least hs_sparse_decode_workspace_bytes(..)
- *            bytes (split-KV partial states); may be NULL when that is 0.
+ *            bytes (split-KV partial states; for the MLA tensor-core kernel
+ *            also one arrival counter per (row, head group), zeroed by the
+ *            call, so that the split that finishes last merges the others in
+ *            its epilogue instead of a second launch); may be NULL when that
+ *            is 0.
  * status     int32 device word or NULL (HS_ERR_TIMEOUT from bounded waits,
  *            HS_ERR_BAD_INDEX from skipped rows).
  * Supported shapes: (d_qk, d_v) = (576, 512) with kv_heads == 1 and k_base
@@ -260,16 +264,23 @@ int hs_sparse_decode_partial(const void* q, const void* k_base, const void* v_ba
  * hs_sparse_decode_partial), and write the final out (bf16 [rows, heads, d_v])
  * and lse (fp32 [rows, heads], natural log, or NULL).  Columns
  * [parts_used, parts_total) may be used as scratch: parts_total must be at
- * least parts_used + hs_sparse_decode_partial_splits(...).  For the MLA shape
- * the merge runs in the attention kernel's epilogue (no extra launch).
+ * least parts_used + hs_sparse_decode_partial_splits(...).
+ * sync: NULL, or int32 scratch of rows * heads words, zeroed by this call on
+ * the stream before the launch.  For the MLA shape on tensor cores, with sync
+ * the new rows are split over several CTAs per (row, group of query heads);
+ * each writes its partial column and the last to finish merges every column
+ * in its epilogue (one launch).  Without sync (or when the split count plus
+ * parts_used exceeds 8 or parts_total) one CTA per (row, head group) attends
+ * and merges in its epilogue.  Other shapes merge with a second launch.
  * ------------------------------------------------------------------------- */
 int hs_sparse_decode_finish(const void* q, const void* k_base, const void* v_base,
                             int64_t row_stride, int64_t kv_head_stride, int64_t num_kv_rows,
                             const int32_t* kv_rows, const int32_t* count, int32_t rows,
                             int32_t cap, int32_t heads, int32_t kv_heads, int32_t d_qk,
                             int32_t d_v, float scale, float* part_m, float* part_l,
-                            float* part_o, int32_t parts_total, int32_t parts_used, void* out,
-                            float* lse, int32_t* status, hs_stream_t stream);
+                            float* part_o, int32_t parts_total, int32_t parts_used,
+                            int32_t* sync, void* out, float* lse, int32_t* status,
+                            hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hs_sparse_decode_noalloc -- the paper has no counterpart; this is a

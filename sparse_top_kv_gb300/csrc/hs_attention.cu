@@ -317,10 +317,20 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     return p;
 }
 
-int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
-    if (p.kind == 0 || p.splits <= 1) return 0;
+// Bytes of the partial states; the tcgen05 kernel also keeps one arrival
+// counter per (row, head group) behind them, 16-byte aligned.
+int64_t partial_bytes(const Plan& p, int rows, int heads, int d_v) {
     const int64_t n = int64_t(rows) * heads;
     return n * p.splits * (2 + int64_t(d_v)) * int64_t(sizeof(float));
+}
+
+int64_t sync_words(const Plan& p, int rows) { return int64_t(rows) * p.chunks_per_kvh; }
+
+int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
+    if (p.kind == 0 || p.splits <= 1) return 0;
+    int64_t b = partial_bytes(p, rows, heads, d_v);
+    if (p.kind == 3) b += (sync_words(p, rows) * 4 + 15) / 16 * 16;
+    return b;
 }
 
 template <int DQK, int DV, int G, bool SHARED, int U>
@@ -356,6 +366,7 @@ struct PartialOut {
     int32_t parts_total;
     int32_t part_base;
     int32_t finish;  // 1: merge with columns [0, part_base) and write out / lse
+    int32_t* sync;   // finish: arrival counters (rows * heads int32) for the last-CTA merge, or null
 };
 
 int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t row_stride,
@@ -381,12 +392,22 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
     const int64_t n = int64_t(rows) * heads;
     AttnArgs a{};
     int combine = 0;
+    int32_t* sync = nullptr;
+    int merge_total = 0;
     Plan pl = p;
     if (po != nullptr) {
         if (po->m == nullptr || po->l == nullptr || po->o == nullptr || po->part_base < 0 ||
             po->part_base > po->parts_total)
             return HS_ERR_INVALID_ARG;
-        if (po->finish && pl.kind == 3 && po->part_base <= 4) {
+        // The last-CTA merge reads part_o in 16-byte vectors.
+        if (po->finish && pl.kind == 3 && po->sync != nullptr && p.splits > 1 &&
+            (reinterpret_cast<uintptr_t>(po->o) & 15u) == 0 &&
+            po->part_base + p.splits <= std::min(po->parts_total, kMlaMaxMerge)) {
+            // Several CTAs per row and head group; the last to finish merges.
+            if (out == nullptr) return HS_ERR_INVALID_ARG;
+            sync = po->sync;
+            merge_total = po->part_base + p.splits;
+        } else if (po->finish && pl.kind == 3 && po->part_base <= 4) {
             // One CTA per row and head group; its epilogue merges.
             pl.splits = 1;
             combine = po->part_base;
@@ -399,7 +420,7 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         a.part_o = po->o;
         a.part_stride = po->parts_total;
         a.part_base = po->part_base;
-        const bool fused = po->finish && pl.kind == 3 && po->part_base <= 4;
+        const bool fused = po->finish && pl.kind == 3 && po->part_base <= 4 && sync == nullptr;
         a.force_partial = fused ? 0 : 1;
     } else {
         const int64_t ws = workspace_bytes(p, rows, heads, d_v);
@@ -409,6 +430,11 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
             a.part_m = w;
             a.part_l = w + n * p.splits;
             a.part_o = w + 2 * n * p.splits;
+            if (p.kind == 3 && p.splits <= kMlaMaxMerge && al(a.part_o)) {
+                sync = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
+                                                  partial_bytes(p, rows, heads, d_v));
+                merge_total = p.splits;
+            }
         }
         a.part_stride = p.splits;
         a.part_base = 0;
@@ -458,8 +484,14 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         m.part_base = a.part_base;
         m.force_partial = a.force_partial;
         m.combine_parts = combine;
+        m.sync = sync;
+        m.merge_total = merge_total;
         m.status = status;
         m.timeout_ns = hs::kWaitTimeoutNs;
+        if (sync != nullptr &&
+            cudaMemsetAsync(sync, 0, size_t(units) * sizeof(int32_t),
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return HS_ERR_CUDA;
         rc = launch_mla_tc(m, p.G, dim3(units, pl.splits), stream);
     } else if (p.kind == 1) {
         rc = launch<576, 512, 4, true, 2>(a, units, stream);
@@ -472,6 +504,7 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         }
     }
     if (rc != HS_OK) return rc;
+    if (sync != nullptr) return rc;  // merged by the last CTA of each (row, head group)
     if (po != nullptr) {
         if (!po->finish || (pl.kind == 3 && po->part_base <= 4)) return rc;
         // Finish on the other kernels: merge every column written so far.
@@ -514,7 +547,7 @@ extern "C" int hs_sparse_decode_partial(const void* q, const void* k_base, const
                                         int32_t d_v, float scale, float* part_m, float* part_l,
                                         float* part_o, int32_t parts_total, int32_t part_base,
                                         int32_t* status, hs_stream_t stream) {
-    const PartialOut po{part_m, part_l, part_o, parts_total, part_base, 0};
+    const PartialOut po{part_m, part_l, part_o, parts_total, part_base, 0, nullptr};
     return decode_impl(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
                        rows, cap, heads, kv_heads, d_qk, d_v, scale, nullptr, nullptr, nullptr, 0,
                        &po, status, stream);
@@ -527,9 +560,9 @@ extern "C" int hs_sparse_decode_finish(const void* q, const void* k_base, const 
                                        int32_t heads, int32_t kv_heads, int32_t d_qk,
                                        int32_t d_v, float scale, float* part_m, float* part_l,
                                        float* part_o, int32_t parts_total, int32_t parts_used,
-                                       void* out, float* lse, int32_t* status,
+                                       int32_t* sync, void* out, float* lse, int32_t* status,
                                        hs_stream_t stream) {
-    const PartialOut po{part_m, part_l, part_o, parts_total, parts_used, 1};
+    const PartialOut po{part_m, part_l, part_o, parts_total, parts_used, 1, sync};
     return decode_impl(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows, count,
                        rows, cap, heads, kv_heads, d_qk, d_v, scale, out, lse, nullptr, 0, &po,
                        status, stream);

@@ -28,9 +28,16 @@ struct MlaArgs {
     int32_t force_partial;    // 1: write partial states even when splits == 1
     int32_t combine_parts;    // >0 (splits == 1): merge with partial columns [0, combine_parts)
                               // in the epilogue and write the final out / lse
+    int32_t* sync;            // per (row, head group) arrival counters, zero on entry, or
+                              // nullptr; with it every split writes its partial column and
+                              // the last one to finish merges columns [0, merge_total)
+    int32_t merge_total;
     int32_t* status;
     uint64_t timeout_ns;
 };
+
+// Columns the last-CTA merge of the tcgen05 kernel can combine.
+constexpr int kMlaMaxMerge = 8;
 
 // Query heads handled by one CTA (64, 32 or 16), or 0 when heads % 16 != 0.
 int mla_tc_head_group(int heads);

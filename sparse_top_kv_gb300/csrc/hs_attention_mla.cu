@@ -57,13 +57,14 @@ constexpr int kMaxCombine = 4;      // partial columns a finishing pass can merg
 constexpr int kQkUnits = 5;         // 4 K pairs + the RoPE block
 constexpr int kPvUnits = 4;         // 4 V pairs
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kBarBytes = 6144;     // shared-memory budget of Bars
 
 template <int HG>
 struct Cfg {
     static constexpr int HH = HG / 2;                  // heads per softmax thread
     static constexpr int kQBytes = kNB * HG * 128;
     static constexpr int kPBytes = 2 * HG * 128;       // P^T: [2 token halves][HG][128 B]
-    static constexpr int kFixed = kQBytes + kPBytes + 4096 + 1024;  // + barriers, alignment
+    static constexpr int kFixed = kQBytes + kPBytes + kBarBytes + 1024;  // + alignment
     static constexpr int NU = (kSmemLimit - kFixed) / kUnit > 6 ? 6 : (kSmemLimit - kFixed) / kUnit;
     static constexpr int kRingOff = 0;
     static constexpr int kQOff = kRingOff + NU * kUnit;
@@ -83,15 +84,20 @@ struct Bars {
     uint64_t pv_done[2];     // PV(t) complete (MMA commit), by t & 1
     uint64_t drain;
     uint64_t group[2];       // barrier of one head half (128 arrivals)
+    uint64_t group_all;      // barrier of the 256 softmax threads
     uint32_t tmem_base;
     int32_t abort;
+    int32_t last;            // this CTA arrived last for its (row, head group)
     uint32_t vote[2][2][4];  // [t & 1][half][quarter]
     float red[2][4][32];     // [half][quarter][head of the half]
     float alpha[2][32];      // O rescale factors of a rescaling tile, [half][head]
     float mref[2][2][32];    // reference maxima (log2 units), [buffer][half][head]
-    float cw[64][6];         // finishing merge, per head: w_own, 1/L_total, w_part[4]
+    // Merge weights per head: the fused finish uses w_own, 1/L_total,
+    // w_part[4]; the last-CTA merge uses w[0 .. kMlaMaxMerge) and 1/L_total
+    // at kMlaMaxMerge.
+    float cw[64][kMlaMaxMerge + 2];
 };
-static_assert(sizeof(Bars) <= 4096, "barrier block");
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             hs::mbar_init(&B.group[i], kHalfThreads);
         }
         hs::mbar_init(&B.p_full, kSoftWarps * 32);
+        hs::mbar_init(&B.group_all, kSoftWarps * 32);
         hs::mbar_init(&B.drain, 1);
         for (int i = 0; i < 64; ++i) B.mref[0][i >> 5][i & 31] = -CUDART_INF_F;
         B.abort = 0;
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
 #pragma unroll
         for (int h = 0; h < HH; ++h) l_part[h] = 0.f;
         int msel = 0;
-        uint32_t gphase = 0;
+        uint32_t gphase = 0, aphase = 0;
         bool ok = true;
         // Bounded barrier of the 128 threads of this head half.
         auto group_sync = [&]() -> bool {
@@ -376,6 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             return (t < T && j < n) ? __ldg(kv_rows + j) : -1;
         };
         int32_t id_next = token_id(0);
+        // Bounded barrier of all 256 softmax threads.
+        auto all_sync = [&]() -> bool {
+            hs::mbar_arrive(&B.group_all);
+            const bool r = hs::mbar_wait_bounded(&B.group_all, aphase & 1, tmo, abort_flag);
+            ++aphase;
+            return r;
+        };
         for (int t = 0; t < T && ok; ++t) {
             const int sb = t & 1;
             const int32_t id_t = id_next;
@@ -604,6 +618,106 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                             } else {
                                 a.part_o[(qh * a.part_stride + a.part_base + split) * 512 + d] =
                                     acc;
+                            }
+                        }
+                    }
+                }
+                // Split merge inside the kernel: every split has written its
+                // partial column; the split that arrives last for this (row,
+                // head group) merges columns [0, merge_total) with eq. (7)
+                // (writes made visible with a fence before the arrival,
+                // partials read from L2 after it).
+                if (a.sync != nullptr) {
+                    __threadfence();
+                    bool last = false;
+                    bool synced = all_sync();
+                    if (synced) {
+                        if (tid == 0) {
+                            const int old = atomicAdd(a.sync + blockIdx.x, 1);
+                            B.last = old == a.splits - 1 ? 1 : 0;
+                        }
+                        synced = all_sync();
+                        last = synced && B.last != 0;
+                    }
+                    if (!synced) {
+                        hs::set_status(a.status, HS_ERR_TIMEOUT);
+                        B.abort = 1;
+                    }
+                    if (last) {
+                        __threadfence();
+                        const int nc = min(a.merge_total, kMlaMaxMerge);
+                        if (ht < HH) {
+                            const int64_t qh = qh0 + hoff + ht;
+                            const int64_t base = qh * a.part_stride;
+                            float* w = B.cw[hoff + ht];
+                            float M = -CUDART_INF_F;
+                            for (int c = 0; c < nc; ++c)
+                                if (__ldcg(a.part_l + base + c) > 0.f)
+                                    M = fmaxf(M, __ldcg(a.part_m + base + c));
+                            float Lt = 0.f;
+                            for (int c = 0; c < kMlaMaxMerge; ++c) {
+                                float wc = 0.f;
+                                if (c < nc && M != -CUDART_INF_F) {
+                                    const float lc = __ldcg(a.part_l + base + c);
+                                    if (lc > 0.f) {
+                                        wc = exp2f(__ldcg(a.part_m + base + c) - M);
+                                        Lt = fmaf(wc, lc, Lt);
+                                    }
+                                }
+                                w[c] = wc;
+                            }
+                            w[kMlaMaxMerge] = Lt > 0.f ? 1.f / Lt : 0.f;
+                            if (a.lse != nullptr)
+                                a.lse[qh] = Lt > 0.f ? (M + log2f(Lt)) * 0.6931471805599453f
+                                                     : -CUDART_INF_F;
+                        }
+                        if (!group_sync()) {
+                            hs::set_status(a.status, HS_ERR_TIMEOUT);
+                            B.abort = 1;
+                        } else {
+                            // 16-byte chunks of d (128 per head), distributed over the
+                            // half's 128 threads; eight chunks in flight per thread.
+                            constexpr int kChunks = HH * 128;
+#pragma unroll 1
+                            for (int e0 = ht; e0 < kChunks; e0 += 8 * kHalfThreads) {
+                                float4 acc[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                for (int c = 0; c < nc; ++c) {
+                                    float4 v[8];
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) {
+                                        const int e = e0 + i * kHalfThreads;
+                                        const int64_t qh = qh0 + hoff + e / 128;
+                                        v[i] = e < kChunks
+                                                   ? __ldcg(reinterpret_cast<const float4*>(
+                                                                a.part_o + (qh * a.part_stride + c) * 512) +
+                                                            (e & 127))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    }
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) {
+                                        const int e = e0 + i * kHalfThreads;
+                                        const float wc = e < kChunks ? B.cw[hoff + e / 128][c] : 0.f;
+                                        acc[i].x = fmaf(wc, v[i].x, acc[i].x);
+                                        acc[i].y = fmaf(wc, v[i].y, acc[i].y);
+                                        acc[i].z = fmaf(wc, v[i].z, acc[i].z);
+                                        acc[i].w = fmaf(wc, v[i].w, acc[i].w);
+                                    }
+                                }
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const int e = e0 + i * kHalfThreads;
+                                    if (e >= kChunks) continue;
+                                    const int hl = hoff + e / 128;
+                                    const float sc = B.cw[hl][kMlaMaxMerge];
+                                    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * sc, acc[i].y * sc);
+                                    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * sc, acc[i].w * sc);
+                                    uint2 pk;
+                                    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                                    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                                    *reinterpret_cast<uint2*>(a.out + (qh0 + hl) * 512 + (e & 127) * 4) = pk;
+                                }
                             }
                         }
                     }

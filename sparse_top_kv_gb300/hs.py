@@ -50,7 +50,7 @@ _SIGS = {
                                   _I32, _I32, _F32, _P, _P, _P, _I32, _I32, _P, _P],
                                  ctypes.c_int),
     "hs_sparse_decode_finish": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
-                                 _I32, _I32, _F32, _P, _P, _P, _I32, _I32, _P, _P, _P, _P],
+                                 _I32, _I32, _F32, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P],
                                 ctypes.c_int),
     "hs_sparse_decode_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
                                   _I32, _I32, _F32, _P, _P, _P, _P], ctypes.c_int),
@@ -267,11 +267,14 @@ def sparse_decode_partial(q, k_base, v_base, row_stride, kv_head_stride, num_kv_
 
 
 def sparse_decode_finish(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows,
-                         count, scale, d_v, part_m, part_l, part_o, parts_used, *, out=None,
-                         lse=None, status=None, stream=None):
+                         count, scale, d_v, part_m, part_l, part_o, parts_used, *, sync=None,
+                         out=None, lse=None, status=None, stream=None):
     """Attend over kv_rows, merge with partial columns [0, parts_used) and
-    write the final (out bf16 [rows, heads, d_v], lse fp32 [rows, heads])."""
+    write the final (out bf16 [rows, heads, d_v], lse fp32 [rows, heads]).
+    sync: optional int32 scratch of rows*heads words (lets the MLA kernel split
+    the rows over several CTAs and merge in the last one)."""
     _check(q, torch.bfloat16, "q")
+    _check(sync, torch.int32, "sync")
     _check(kv_rows, torch.int32, "kv_rows")
     _check(count, torch.int32, "count")
     for t, n in ((part_m, "part_m"), (part_l, "part_l"), (part_o, "part_o")):
@@ -286,7 +289,7 @@ def sparse_decode_finish(q, k_base, v_base, row_stride, kv_head_stride, num_kv_r
     _call("hs_sparse_decode_finish", _ptr(q), _ptr(k_base), _ptr(v_base), row_stride,
           kv_head_stride, num_kv_rows, _ptr(kv_rows), _ptr(count), rows, cap, heads, kv_heads,
           d_qk, d_v, float(scale), _ptr(part_m), _ptr(part_l), _ptr(part_o), part_m.shape[-1],
-          parts_used, _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+          parts_used, _ptr(sync), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
     return out, lse
 
 

@@ -68,6 +68,8 @@ class HiSparseDecoder:
         self.parts_miss = self.parts_hit
         P = self.parts_hit + self.parts_miss
         f32 = dict(dtype=torch.float32, device=dev)
+        # Arrival counters of the finishing pass's last-CTA merge.
+        self.sync = torch.zeros(R * heads, dtype=torch.int32, device=dev)
         self.part_m = torch.empty(R * heads, P, **f32)
         self.part_l = torch.empty(R * heads, P, **f32)
         self.part_o = torch.empty(R * heads, P, d_v, **f32)
@@ -168,8 +170,8 @@ class HiSparseDecoder:
         hs.sparse_decode_finish(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                 miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),
                                 self.scale, self.d_v, self.part_m, self.part_l, self.part_o,
-                                self.parts_hit, out=self.out, lse=self.lse, status=self.status,
-                                stream=main)
+                                self.parts_hit, sync=self.sync, out=self.out, lse=self.lse,
+                                status=self.status, stream=main)
         rec(6, main)
         return self.out, self.lse
 

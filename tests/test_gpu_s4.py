@@ -156,6 +156,11 @@ def test_partial_passes_merge_to_the_full_set(heads, d):
     # The fused last pass: the second half attended and merged in one call.
     out2, lse2 = hs.sparse_decode_finish(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb),
                                          1 / math.sqrt(d), d_v, pm, pl, po, pa, status=status)
+    # The split last pass: several CTAs per row, the last to arrive merges.
+    sync = torch.full((rows * H,), 7, dtype=torch.int32, device="cuda")  # zeroed by the call
+    out3, lse3 = hs.sparse_decode_finish(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb),
+                                         1 / math.sqrt(d), d_v, pm, pl, po, pa, sync=sync,
+                                         status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
     sample = [0, 7, rows - 1]
@@ -166,6 +171,7 @@ def test_partial_passes_merge_to_the_full_set(heads, d):
     idx = torch.tensor(sample, device="cuda")
     check_attention(out.view(rows, H, d_v)[idx], lse.view(rows, H)[idx], ref_out, ref_lse)
     check_attention(out2[idx], lse2[idx], ref_out, ref_lse, label="finish")
+    check_attention(out3[idx], lse3[idx], ref_out, ref_lse, label="finish with split merge")
 
 
 def test_merge_states_kernel():
