@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 from sparse_top_kv_gb300 import hs, inputs, replicas  # noqa: E402
 from sparse_top_kv_gb300.pipeline import HiSparseDecoder  # noqa: E402
 
-L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_BYTES = 512 << 20
 ROW_BYTES = 1152
 # DRAM bytes per launch from the ncu capture summarised in profiles/ (null when
 # the kernel changed after the capture).
@@ -47,7 +47,8 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled around and during the
+    timed region (a reader thread collects the lines)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -57,8 +58,16 @@ class ClockSampler:
         self.proc = None
         self.device = device
         self.lines = []
+        self.thread = None
 
-    def start(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+
+    def start(self, first_sample_timeout=10.0):
+        """Start sampling and return once the first sample has been read, so
+        that the tool's own start-up lies outside the timed region."""
+        import threading
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "200"]
         try:
@@ -71,16 +80,27 @@ class ClockSampler:
                                          text=True)
         except Exception:
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < first_sample_timeout:
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=5)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -133,17 +153,40 @@ def device_inputs(cfg, dec):
                 new_rows=cfg["new_rows"].cuda())
 
 
-def run_full(args, rank, world, flush):
-    """Step 0 (the all-miss cold step) runs eagerly, which also performs the
-    library's one-time set-up; the step is then captured once as a CUDA graph
-    over static input buffers.  Warm-up steps 1..W-1 and the K timed steps
-    copy their device-resident inputs into those buffers and replay the graph.
-    Timing events inside the graph give the per-stage breakdown."""
-    S = args.warmup + args.steps
-    cfg = setup_full(S, rank)
+def warm_host_memory(cfg, steps):
+    """Set-up, untimed: a throwaway decoder steps once through the workload,
+    so that the host-pool pages the timed steps read (including the rows
+    BackUp writes) have been read by the GPU before (first GPU reads of host
+    pages are slow on these machines).  The timed decoder starts from a cold
+    hot buffer and LRU state all the same."""
     dec = make_decoder(cfg)
     dec.warm_pool()
     di = device_inputs(cfg, dec)
+    for s in range(steps):
+        dec.step(di["cand"][s], di["seq"][s], di["newest"][s], di["new_rows"][s], di["q"][s])
+    torch.cuda.synchronize()
+    assert int(dec.status.item()) == 0
+    del dec, di
+    torch.cuda.empty_cache()
+
+
+def run_full(args, rank, world, flush):
+    """Step 0 (the all-miss cold step) runs eagerly, which also performs the
+    library's one-time set-up; the step is then captured as a CUDA graph over
+    static input buffers.  Warm-up steps 1..W-1 and the K timed steps copy
+    their device-resident packed inputs into those buffers (one copy) and
+    replay the graph.  The per-stage breakdown comes from a second graph of
+    the same step with timing events inside, replayed over the same K steps
+    after the decoder state (hot buffer, dgi, lru, stats) is restored to its
+    value before the timed steps; those events are not in the timed steps."""
+    S = args.warmup + args.steps
+    cfg = setup_full(S, rank)
+    warm_host_memory(cfg, S)
+    dec = make_decoder(cfg)
+    dec.warm_pool()
+    di = device_inputs(cfg, dec)
+    packed = [dec.pack_inputs(di["cand"][s], di["seq"][s], di["newest"][s], di["new_rows"][s],
+                              di["q"][s]) for s in range(S)]
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     flush_l2(flush)
@@ -154,23 +197,20 @@ def run_full(args, rank, world, flush):
         gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
     except TypeError:
         gev = None
-    dec.capture(events=gev)
+    g_events = dec.capture(events=gev) if gev is not None else None
+    g_plain = dec.capture()
     torch.cuda.synchronize()
-
-    def run(s):
-        return dec.replay(di["cand"][s], di["seq"][s], di["newest"][s], di["new_rows"][s],
-                          di["q"][s])
 
     for s in range(1, args.warmup):
         flush_l2(flush)
-        run(s)
+        dec.replay_packed(packed[s])
     torch.cuda.synchronize()
+    snapshot = (dec.hot.clone(), dec.dgi.clone(), dec.lru.clone(), dec.stats.clone())
     clocks = ClockSampler(torch.cuda.current_device())
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    stage_ms = np.zeros(7)
     total_ms = 0.0
     miss_total = hit_total = 0
     step_ms = []
@@ -179,7 +219,7 @@ def run_full(args, rank, world, flush):
         a, b = ev(), ev()
         st0 = dec.stats.clone()
         a.record(stream)
-        run(s)
+        dec.replay_packed(packed[s])
         b.record(stream)
         b.synchronize()
         step_ms.append(a.elapsed_time(b))
@@ -187,23 +227,39 @@ def run_full(args, rank, world, flush):
         d = dec.stats - st0
         hit_total += int(d[0])
         miss_total += int(d[1])
-        if gev is not None:
-            e = lambda i, j: gev[i].elapsed_time(gev[j])  # noqa: E731
-            stage_ms += np.array([e(0, 1), e(1, 2), e(2, 3), e(3, 4), e(2, 5),
-                                  min(e(4, 6), e(5, 6)), e(0, 6)])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    swap_bytes = miss_total * ROW_BYTES
     assert int(dec.status.item()) == 0, f"device status {dec.status.item()}"
+    # Stage breakdown: the same K steps again from the same state, through
+    # the graph with events (untimed as a whole).
+    stage_ms = np.zeros(7)
+    if g_events is not None:
+        for t, v in zip((dec.hot, dec.dgi, dec.lru, dec.stats), snapshot):
+            t.copy_(v)
+        dec.graph = g_events
+        for s in range(args.warmup, S):
+            flush_l2(flush)
+            dec.replay_packed(packed[s])
+            torch.cuda.synchronize()
+            e = lambda i, j: gev[i].elapsed_time(gev[j])  # noqa: E731
+            # S1, S2, BackUp, SwapIn (side stream, after S2), resident rows,
+            # swapped rows + merge, whole step.
+            stage_ms += np.array([e(0, 1), e(1, 2), e(2, 3), e(3, 4), e(2, 5),
+                                  min(e(4, 6), e(5, 6)), e(0, 6)])
+        dec.graph = g_plain
+        assert int(dec.status.item()) == 0, f"device status {dec.status.item()}"
+    del snapshot
+    swap_bytes = miss_total * ROW_BYTES
     total_ms = replicas.max_over_ranks(total_ms)
     K = args.steps
     res = dict(total_ms=total_ms, K=K, stage_ms=(stage_ms / K).tolist(),
                hit_rate=hit_total / max(1, hit_total + miss_total),
                hit_rows_per_step=hit_total / K, step_ms=step_ms,
-               stage_src="timing events inside the captured step graph" if gev is not None
-               else "not available (no external events in this torch)",
+               stage_src="a graph of the same step with timing events inside, replayed over "
+                         "the same steps from the same state after the timed run"
+               if g_events is not None else "not available (no external events in this torch)",
                swap_bytes_per_step=swap_bytes / K, clocks=clk, cfg=cfg, dec=dec, di=di,
                launches=dec.launches_per_step() * K)
     return res
@@ -211,17 +267,19 @@ def run_full(args, rank, world, flush):
 
 def run_e2e(args, cfg, flush):
     """Same steps through the public API with the step's inputs in pinned host
-    memory: every timed step copies its inputs (indices, q, new rows, lengths,
-    slots) host -> device into the captured step's input buffers, replays the
-    step and copies out + lse device -> host."""
+    memory: every timed step copies its packed inputs (indices, lengths,
+    slots, new rows, q) host -> device into the captured step's input buffer
+    (one copy), replays the step and copies out + lse device -> host."""
     S = args.warmup + args.steps
     dec = make_decoder(cfg)
     dec.warm_pool()
     di_dev = device_inputs(cfg, dec)
-    host = {k: v.cpu().pin_memory() for k, v in di_dev.items()}
+    host = [dec.pack_inputs(di_dev["cand"][s], di_dev["seq"][s], di_dev["newest"][s],
+                            di_dev["new_rows"][s], di_dev["q"][s]).cpu().pin_memory()
+            for s in range(S)]
     out_h = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
     lse_h = torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory()
-    h2d = sum(v[0].numel() * v[0].element_size() for v in host.values())
+    h2d = host[0].numel()
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     stream = torch.cuda.current_stream()
     total = 0.0
@@ -235,14 +293,14 @@ def run_e2e(args, cfg, flush):
         flush_l2(flush)
         e0, e1 = ev(), ev()
         e0.record(stream)
-        out, lse = dec.replay(host["cand"][s], host["seq"][s], host["newest"][s],
-                              host["new_rows"][s], host["q"][s])
+        out, lse = dec.replay_packed(host[s])
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if s >= args.warmup:
             total += e0.elapsed_time(e1)
+    assert int(dec.status.item()) == 0, f"device status {dec.status.item()}"
     return dict(total_ms=replicas.max_over_ranks(total), h2d=h2d, d2h=d2h)
 
 
@@ -574,7 +632,7 @@ def main():
     stage = full["stage_ms"]
     # Roofline of the dominant kernel of the step: the resident-row attention
     # pass (HBM) runs concurrently with the SwapIn (host link).
-    attn_ms, swap_ms = stage[4], stage[2]
+    attn_ms, swap_ms = stage[4], stage[3]
     hits_per_step = full["hit_rows_per_step"]
     attn_bytes = int(hits_per_step * ROW_BYTES + 64 * 16 * 576 * 2 + 64 * 16 * 2 * 514 * 4
                      + 64 * 2048 * 4)
@@ -622,13 +680,13 @@ def main():
                                "4097 rows/request, 85% reuse + Zipf(1.1)",
                    "global_batch": 64 * world, "seq_len": 131072,
                    "parallelism": f"replicas x{world} (request partition)",
-                   "l2": "flushed (256 MB write) between timed steps, outside the events"},
+                   "l2": "flushed (512 MB write) between timed steps, outside the events"},
         "step_us_timed": [round(x * 1e3, 1) for x in full["step_ms"]],
         "stage_us_note": "timed steps replay one CUDA graph per step; stage_us from "
                          + full["stage_src"],
         "stage_us": {"s1_normalize": stage[0] * 1e3, "s2_lookup": stage[1] * 1e3,
-                     "s3_swap_in (side stream)": stage[2] * 1e3,
-                     "backup (side stream)": stage[3] * 1e3,
+                     "backup (side stream)": stage[2] * 1e3,
+                     "s3_swap_in (side stream)": stage[3] * 1e3,
                      "s4_resident_rows (overlaps the swap)": stage[4] * 1e3,
                      "s4_swapped_rows_and_merge": stage[5] * 1e3, "step": stage[6] * 1e3},
         "hit_rate": full["hit_rate"],

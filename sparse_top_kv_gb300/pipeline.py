@@ -74,7 +74,6 @@ class HiSparseDecoder:
         self.part_l = torch.empty(R * heads, P, **f32)
         self.part_o = torch.empty(R * heads, P, d_v, **f32)
         self.side = torch.cuda.Stream(device=dev)
-        self.ev_newrow = torch.cuda.Event()
         self.ev_lists = torch.cuda.Event()
         self.ev_swapped = torch.cuda.Event()
         # SMs left to the SwapIn while the resident-row attention runs (one
@@ -84,25 +83,30 @@ class HiSparseDecoder:
         attn_ctas = R * max(1, heads // hg) * max(1, self.parts_hit)
         self.swap_ctas = max(32, 2 * (sms - attn_ctas))
 
-    def warm_pool(self, page_bytes=65536):
+    def warm_pool(self, page_bytes=4096):
         """One-time set-up pass: read one row of every `page_bytes` of the host
-        pool into the (still empty) hot buffer with hs_swap_in.
+        pool (every 4 KB page by default) into the (still empty) hot buffer
+        with hs_swap_in, in chunks of at most the hot buffer's rows.
 
         Measured on the GB300 machines used here (VMs whose GPU reaches host
-        memory through the IOMMU): the first GPU reads of a freshly allocated
-        pinned pool run 5-20x below the link rate, for the first ~10^5 rows,
-        then settle at the link rate.  A server pays that once at start-up; this
-        pass pays it at set-up so that a decode step sees the steady state.
-        Must run before the first step (it overwrites hot rows, which are
-        empty until then)."""
+        memory through the IOMMU): the first GPU reads of a page of a freshly
+        allocated pinned pool run far below the link rate; a decoder whose
+        pool had only one row per 64 KB read beforehand ran its first steps
+        3x slower than a later decoder over the same pool.  A server pays that
+        once at start-up; this pass pays it at set-up so that a decode step
+        sees the steady state.  Must run before the first step (it overwrites
+        hot rows, which are empty until then)."""
         stride = max(1, page_bytes // self.row_bytes)
-        src = torch.arange(0, self.host_rows, stride, dtype=torch.int32, device=self.device)
-        n = min(src.numel(), self.hot.shape[0])
-        src = src[:n].view(1, n).contiguous()
-        dst = torch.arange(n, dtype=torch.int64, device=self.device).view(1, n)
-        cnt = torch.full((1,), n, dtype=torch.int32, device=self.device)
-        hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, src, dst, cnt,
-                   status=self.status)
+        chunk = self.hot.shape[0]
+        for r0 in range(0, self.host_rows, stride * chunk):
+            src = torch.arange(r0, min(self.host_rows, r0 + stride * chunk), stride,
+                               dtype=torch.int32, device=self.device)
+            n = src.numel()
+            src = src.view(1, n).contiguous()
+            dst = torch.arange(n, dtype=torch.int64, device=self.device).view(1, n)
+            cnt = torch.full((1,), n, dtype=torch.int32, device=self.device)
+            hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, src, dst, cnt,
+                       status=self.status)
         self.hot.zero_()
         torch.cuda.synchronize(self.device)
 
@@ -123,8 +127,8 @@ class HiSparseDecoder:
         attention over the swapped rows (miss_rows) follows the SwapIn, and the
         two sets of partial states are merged with eq. (7).
         `events`, if given, is a list of 7 CUDA events recorded before S1, after
-        S1, after S2, after BackUp + SwapIn (side stream), again after them,
-        after the resident-row attention and at the end of the step."""
+        S1, after S2, after BackUp and after SwapIn (side stream), after the
+        resident-row attention and at the end of the step."""
         R = self.num_reqs
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side
@@ -144,17 +148,16 @@ class HiSparseDecoder:
                                            stream=main)
         rec(2, main)
         self.ev_lists.record(main)
-        # Side stream: host-link traffic, after S2 (a copy to host memory that
-        # shares an SM with S1 or S2 stalls them).  BackUp needs only the new
-        # rows, written before S1.
+        # Side stream: host-link traffic.  BackUp runs here rather than beside
+        # S1/S2 (measured: a step is ~6 us shorter this way).
         side.wait_event(self.ev_lists)
         hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
                   self.host_rows, status=self.status, stream=side)
+        rec(3, side)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
                    region_stride=self.region_stride, max_ctas=self.swap_ctas,
                    status=self.status, stream=side)
-        rec(3, side)
         rec(4, side)
         self.ev_swapped.record(side)
         # Main stream: HBM traffic over the resident rows meanwhile.
@@ -175,20 +178,49 @@ class HiSparseDecoder:
         rec(6, main)
         return self.out, self.lse
 
+    def _input_layout(self):
+        """Byte layout of one step's inputs packed in one buffer: (name,
+        offset, shape, dtype) per input, 256-byte aligned."""
+        R = self.num_reqs
+        specs = [("cand", (R, self.top_k), torch.int32), ("seq", (R,), torch.int32),
+                 ("newest", (R,), torch.int32), ("new_row", (R, self.row_width), self.hot.dtype),
+                 ("q", (R, self.heads, self.d_qk), torch.bfloat16)]
+        out, off = [], 0
+        for name, shape, dt in specs:
+            n = 1
+            for x in shape:
+                n *= x
+            nbytes = n * torch.empty(0, dtype=dt).element_size()
+            out.append((name, off, shape, dt, nbytes))
+            off += (nbytes + 255) // 256 * 256
+        return out, off
+
+    def pack_inputs(self, cand, seq_lens, newest_slot, new_row, q, out=None):
+        """One step's inputs in the packed layout of `replay_packed` (a uint8
+        tensor on the same device as the given tensors)."""
+        layout, total = self._input_layout()
+        if out is None:
+            out = torch.empty(total, dtype=torch.uint8, device=cand.device)
+        for (name, off, shape, dt, nbytes), t in zip(layout, (cand, seq_lens, newest_slot,
+                                                              new_row, q)):
+            out[off:off + nbytes].view(dt).view(shape).copy_(t.reshape(shape))
+        return out
+
     def capture(self, events=None):
-        """Capture one decode step over static input buffers (`self.graph_in`)
-        as a CUDA graph, both streams included.  `replay(...)` then copies a
-        step's inputs into those buffers and runs the step with one graph
+        """Capture one decode step over static input buffers (`self.graph_in`,
+        views of the packed buffer `self.graph_in_packed`) as a CUDA graph,
+        both streams included.  `replay(...)` / `replay_packed(...)` then copy
+        a step's inputs into those buffers and run the step with one graph
         launch.  Run at least one eager step first (it performs the one-time
         library set-up that capture must not do).  `events`, if given, are
-        timing events recorded inside the graph (see `step`)."""
-        R, dev = self.num_reqs, self.device
-        self.graph_in = dict(
-            cand=torch.empty(R, self.top_k, dtype=torch.int32, device=dev),
-            seq=torch.empty(R, dtype=torch.int32, device=dev),
-            newest=torch.empty(R, dtype=torch.int32, device=dev),
-            new_row=torch.empty(R, self.row_width, dtype=self.hot.dtype, device=dev),
-            q=torch.empty(R, self.heads, self.d_qk, dtype=torch.bfloat16, device=dev))
+        timing events recorded inside the graph (see `step`).  Returns the
+        graph (also kept as self.graph, the one replay uses)."""
+        dev = self.device
+        if getattr(self, "graph_in_packed", None) is None:
+            layout, total = self._input_layout()
+            self.graph_in_packed = torch.empty(total, dtype=torch.uint8, device=dev)
+            self.graph_in = {name: self.graph_in_packed[off:off + nb].view(dt).view(shape)
+                             for name, off, shape, dt, nb in layout}
         gi = self.graph_in
         g = torch.cuda.CUDAGraph()
         self.side.wait_stream(torch.cuda.current_stream(dev))
@@ -206,6 +238,14 @@ class HiSparseDecoder:
         gi["newest"].copy_(newest_slot, non_blocking=True)
         gi["new_row"].copy_(new_row, non_blocking=True)
         gi["q"].copy_(q, non_blocking=True)
+        self.graph.replay()
+        return self.out, self.lse
+
+    def replay_packed(self, packed):
+        """One decode step through the captured graph, the step's inputs given
+        as one packed buffer (`pack_inputs`; device or pinned host memory):
+        one copy, one graph launch."""
+        self.graph_in_packed.copy_(packed, non_blocking=True)
         self.graph.replay()
         return self.out, self.lse
 
