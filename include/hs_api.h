@@ -159,7 +159,7 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
  * row_bytes   multiple of 16 ([HS] HiSparseCoordinator rejects others).
  * miss_src/miss_dst/miss_count  as produced by hs_hot_lookup_assign.
  * dgi         int32 [rows, hot_size] or NULL: revocation target.
- * max_ctas    CTAs the copy may occupy (0 = two per SM).  A smaller budget
+ * max_ctas    SMs the copy may occupy, one CTA each (0 = every SM).  A smaller budget
  *             leaves SMs to a kernel running concurrently on another stream
  *             ([HC] Motivation: the copy's SM footprint is the cost to the
  *             concurrent forward pass); a few dozen CTAs already keep enough

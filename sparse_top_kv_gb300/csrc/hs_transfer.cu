@@ -30,8 +30,11 @@
 namespace {
 
 // Each warp owns a ring of kWS stages of kStageBytes in shared memory and
-// copies groups of up to kMaxGroup consecutive rows of one list.
-constexpr int kWarps = 4;
+// copies groups of up to kMaxGroup consecutive rows of one list.  Eight
+// warps' rings (192 KB) fill an SM's shared memory, so a CTA budget is an SM
+// budget: the copy never takes a slice of many SMs that a concurrent kernel
+// with large CTAs then cannot use.
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWS = 3;
 constexpr uint32_t kStageBytes = 8192;
@@ -230,8 +233,8 @@ int launch_xfer(XferArgs a, int64_t max_items_rows, int max_ctas, hs_stream_t st
     if (rc != HS_OK) return rc;
     a.group = int32_t(hs::max64(1, hs::min64(kMaxGroup, int64_t(kStageBytes) / a.row_bytes)));
     const int64_t groups = (max_items_rows + a.group - 1) / a.group;
-    // Two CTAs (96 KB of stages each) fit one SM.
-    const int64_t budget = max_ctas > 0 ? max_ctas : 2 * int64_t(hs_host::num_sms());
+    // One CTA (192 KB of stages) per SM.
+    const int64_t budget = max_ctas > 0 ? max_ctas : int64_t(hs_host::num_sms());
     const int64_t grid = hs::max64(1, hs::min64((groups + kWarps - 1) / kWarps, budget));
     xfer_kernel<<<int(grid), kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();
