@@ -31,9 +31,10 @@ from sparse_top_kv_gb300.pipeline import HiSparseDecoder  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
 ROW_BYTES = 1152
-# DRAM bytes per launch from the ncu capture summarised in profiles/ (null when
-# the kernel changed after the capture).
-NCU_TRAFFIC = {"attention": None, "swap_in": None}
+# DRAM bytes (read + write) per launch from the ncu capture summarised in
+# profiles/step_kernels_full_hisparse.md (set to None when a kernel changes
+# after the capture).
+NCU_TRAFFIC = {"attention": 131856640 + 19920384, "swap_in": 266752 + 9644544}
 
 
 def load_peaks():

@@ -111,39 +111,74 @@ __global__ void __launch_bounds__(kThreads) attn_cc_kernel(const AttnArgs a) {
     const char* vb = reinterpret_cast<const char*>(a.v) + int64_t(kvh) * a.head_stride * 2;
     bool bad = false;
 
-    for (int j0 = t0 + warp * U; j0 < t1; j0 += kWarps * U) {
-        int64_t rowsel[U];
+    // Software pipeline per warp: the row ids of iteration it+2 and the K/V
+    // rows of iteration it+1 are in flight while iteration it is computed.
+    constexpr int kStep = kWarps * U;
+    int32_t id_n2[U];   // ids two iterations ahead
+    int64_t rs_n[U];    // rows one iteration ahead
+    uint32_t kr_n[U][NQ];
+    uint32_t vr_n[U][SHARED_KV ? 1 : NV];
+    auto load_ids = [&](int j0, int32_t (&id)[U]) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = j0 + u;
-            int64_t r = j < t1 ? int64_t(__ldg(a.kv_rows + idx_base + j)) : -1;
+            id[u] = j < t1 ? __ldg(a.kv_rows + idx_base + j) : -1;
+        }
+    };
+    auto load_rows = [&](const int32_t (&id)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            int64_t r = id[u];
             if (r >= a.num_kv_rows) { bad = true; r = -1; }
             if (r < 0) r = -1;
-            rowsel[u] = r;
+            rs_n[u] = r;
+            if (r >= 0) {  // warp-uniform branch
+                const uint32_t* kp = reinterpret_cast<const uint32_t*>(kb + r * a.row_stride * 2);
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) kr_n[u][i] = __ldg(kp + 32 * i + lane);
+                if constexpr (!SHARED_KV) {
+                    const uint32_t* vp =
+                        reinterpret_cast<const uint32_t*>(vb + r * a.row_stride * 2);
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) vr_n[u][i] = __ldg(vp + 32 * i + lane);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) kr_n[u][i] = 0u;
+                if constexpr (!SHARED_KV) {
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) vr_n[u][i] = 0u;
+                }
+            }
         }
+    };
+    {
+        int32_t id0[U];
+        load_ids(t0 + warp * U, id0);
+        load_ids(t0 + warp * U + kStep, id_n2);
+        load_rows(id0);
+    }
+    for (int j0 = t0 + warp * U; j0 < t1; j0 += kStep) {
+        // Current iteration's rows, then start the next iteration's loads.
+        int64_t rowsel[U];
         uint32_t kr[U][NQ];
         uint32_t vr[U][SHARED_KV ? 1 : NV];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (rowsel[u] >= 0) {  // warp-uniform branch
-                const uint32_t* kp =
-                    reinterpret_cast<const uint32_t*>(kb + rowsel[u] * a.row_stride * 2);
+            rowsel[u] = rs_n[u];
 #pragma unroll
-                for (int i = 0; i < NQ; ++i) kr[u][i] = __ldg(kp + 32 * i + lane);
-                if constexpr (!SHARED_KV) {
-                    const uint32_t* vp =
-                        reinterpret_cast<const uint32_t*>(vb + rowsel[u] * a.row_stride * 2);
+            for (int i = 0; i < NQ; ++i) kr[u][i] = kr_n[u][i];
+            if constexpr (!SHARED_KV) {
 #pragma unroll
-                    for (int i = 0; i < NV; ++i) vr[u][i] = __ldg(vp + 32 * i + lane);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NQ; ++i) kr[u][i] = 0u;
-                if constexpr (!SHARED_KV) {
-#pragma unroll
-                    for (int i = 0; i < NV; ++i) vr[u][i] = 0u;
-                }
+                for (int i = 0; i < NV; ++i) vr[u][i] = vr_n[u][i];
             }
+        }
+        if (j0 + kStep < t1) {
+            int32_t id1[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) id1[u] = id_n2[u];
+            load_ids(j0 + 2 * kStep, id_n2);
+            load_rows(id1);
         }
         float s[U][G];
 #pragma unroll
@@ -309,7 +344,8 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     }
     p.chunks_per_kvh = group / p.G;
     const int64_t units = int64_t(rows) * kv_heads * p.chunks_per_kvh;
-    const int64_t target = 2LL * hs_host::num_sms();
+    // Enough CTAs (up to four per SM) to keep many rows in flight.
+    const int64_t target = 4LL * hs_host::num_sms();
     int64_t s = (target + units - 1) / units;
     s = hs::min64(s, std::max(1, cap / 32));
     s = hs::max64(1, hs::min64(s, 64));
