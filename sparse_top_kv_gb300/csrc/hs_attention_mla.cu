@@ -481,7 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                     break;
                 }
             }
-            // P^T tile, bf16, K-major: row h, token column qd*32 + lane.
+            // P^T tile, bf16, K-major: row h, token column qd*32 + lane.  The
+            // reference maxima are copied to registers first: read through the
+            // shared-memory pointer inside the loop, each load would have to
+            // wait for the P stores before it (possible aliasing).
+            float mr[HH];
+#pragma unroll
+            for (int h = 0; h < HH; ++h) mr[h] = m_ref[h];
             const int tok = qd * 32 + lane;
             unsigned char* prow = smem + C::kPOff + (tok >> 6) * HG * 128;
             const int tcol = (tok & 63) * 2;
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             for (int h = 0; h < HH; ++h) {
                 const int hg = hoff + h;
                 // A masked logit contributes 0 (also while m_ref is still -inf).
-                const float p = s[h] == -CUDART_INF_F ? 0.f : exp2f(s[h] - m_ref[h]);
+                const float p = s[h] == -CUDART_INF_F ? 0.f : exp2f(s[h] - mr[h]);
                 const __nv_bfloat16 pb = __float2bfloat16_rn(p);
                 l_part[h] += __bfloat162float(pb);
                 *reinterpret_cast<__nv_bfloat16*>(
