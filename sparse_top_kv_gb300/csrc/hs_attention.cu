@@ -344,9 +344,12 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     }
     p.chunks_per_kvh = group / p.G;
     const int64_t units = int64_t(rows) * kv_heads * p.chunks_per_kvh;
-    // Enough CTAs (up to four per SM) to keep many rows in flight.
-    const int64_t target = 4LL * hs_host::num_sms();
-    int64_t s = (target + units - 1) / units;
+    // GQA: one resident wave (two CTAs per SM, one for a group of 8), so that
+    // longer CTAs amortise the Q load, the epilogue and the merge.  MLA on
+    // CUDA cores: up to four CTAs per SM.
+    const int64_t per_sm = p.kind == 2 ? (p.G >= 8 ? 1 : 2) : 4;
+    const int64_t target = per_sm * hs_host::num_sms();
+    int64_t s = hs::max64(1, target / units);
     s = hs::min64(s, std::max(1, cap / 32));
     s = hs::max64(1, hs::min64(s, 64));
     p.splits = int(s);
@@ -367,6 +370,254 @@ int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
     int64_t b = partial_bytes(p, rows, heads, d_v);
     if (p.kind == 3) b += (sync_words(p, rows) * 4 + 15) / 16 * 16;
     return b;
+}
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// GQA rows of 128 bf16 with K and V in separate caches: a half-warp per
+// candidate row.  Lane l of a half holds d = 8 l .. 8 l + 7 of the row (one
+// 16-byte piece of K and one of V); a (row, head) dot product is 8 FMAs and a
+// 4-step shuffle butterfly inside the half, so every shuffle serves the two
+// rows of a warp.  Each half-warp keeps its own online-softmax state (eqs.
+// 4-6) over its rows; the 16 states of the CTA are merged with eq. (7).
+//
+// Loads: the CTA's candidate ids are staged in shared memory (one coalesced
+// read per chunk of kIdChunk), and every lane streams its own 16-byte pieces
+// of K and V through a private S-stage cp.async ring in shared memory, so
+// S - 1 iterations of U rows per half-warp are in flight while one is
+// computed.  A lane reads back only what it copied itself: the cp.async
+// group wait of the thread is the only synchronisation the ring needs.
+constexpr int kIdChunk = 2048;
+
+template <int G, int U, int S>
+constexpr size_t gqa_smem_bytes() {
+    constexpr size_t ring = size_t(kWarps) * 2 * S * U * 2 * 256;
+    constexpr size_t reduce = size_t(kWarps) * 2 * G * (128 + 2) * sizeof(float);
+    return kIdChunk * sizeof(int32_t) + (ring > reduce ? ring : reduce);
+}
+
+template <int G, int U, int S>
+__global__ void __launch_bounds__(kThreads, G >= 8 ? 1 : 2) attn_gqa_kernel(const AttnArgs a) {
+    constexpr int D = 128;
+    constexpr int kVW = kWarps * 2;               // row streams (half-warps) per CTA
+    extern __shared__ __align__(16) unsigned char gsm[];
+    int32_t* ids = reinterpret_cast<int32_t*>(gsm);                    // [kIdChunk]
+    unsigned char* ring = gsm + kIdChunk * sizeof(int32_t);            // [kVW][S][U][K,V][256 B]
+    float* red = reinterpret_cast<float*>(ring);  // after the loop: [kVW][G][D] + m, l [kVW][G]
+
+    const int unit = blockIdx.x;
+    const int split = blockIdx.y;
+    const int chunk = unit % a.chunks_per_kvh;
+    const int kvh = (unit / a.chunks_per_kvh) % a.kv_heads;
+    const int row = unit / (a.chunks_per_kvh * a.kv_heads);
+    const int group = a.heads / a.kv_heads;
+    const int h0 = kvh * group + chunk * G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hl = lane & 15;                     // lane within the half-warp
+    const int vw = warp * 2 + (lane >> 4);        // row stream of this half-warp
+
+    auto unpack8 = [](const uint4& u, float (&f)[8]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    };
+    // Query slice, pre-scaled into the exp2 domain.
+    float q[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                                    a.q + (int64_t(row) * a.heads + h0 + h) * D) + hl);
+        unpack8(raw, q[h]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[h][e] *= a.scale_log2;
+    }
+    float o[G][8];
+    float m[G], l[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -CUDART_INF_F;
+        l[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+    }
+
+    const int64_t idx_base = (int64_t(row) * a.kv_heads + kvh) * a.cap;
+    const int n = a.count ? min(max(a.count[int64_t(row) * a.kv_heads + kvh], 0), a.cap) : a.cap;
+    const int per = (n + a.splits - 1) / a.splits;
+    const int t0 = min(n, split * per), t1 = min(n, t0 + per);
+    const char* kb = reinterpret_cast<const char*>(a.k) + int64_t(kvh) * a.head_stride * 2;
+    const char* vb = reinterpret_cast<const char*>(a.v) + int64_t(kvh) * a.head_stride * 2;
+    const uint32_t ring_me = hs::smem_u32(ring) + uint32_t(vw) * (S * U * 512) + hl * 16;
+    constexpr int kStep = kVW * U;                // rows per CTA iteration
+    bool bad = false;
+
+    // A staged id is the cache row, or -1 when the candidate is not live
+    // (padding, or out of the cache's range: flagged, contributes nothing).
+    for (int c0 = t0; c0 < t1; c0 += kIdChunk) {
+        const int cn = min(kIdChunk, t1 - c0);
+        __syncthreads();  // the previous chunk's ids are no longer read
+        for (int i = threadIdx.x; i < cn; i += kThreads) {
+            const int32_t r = __ldg(a.kv_rows + idx_base + c0 + i);
+            if (r >= a.num_kv_rows) bad = true;
+            ids[i] = r < a.num_kv_rows ? r : -1;
+        }
+        __syncthreads();
+        // Both halves of a warp run the same number of iterations (the dot
+        // products shuffle across the whole warp); rows past cn are not live.
+        const int niter = (cn + kStep - 1) / kStep;
+        auto issue = [&](int it) {
+            const uint32_t st = ring_me + uint32_t(it % S) * (U * 512);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = it * kStep + vw * U + u;
+                const int32_t r = j < cn ? ids[j] : -1;
+                const int64_t off = r >= 0 ? int64_t(r) * a.row_stride * 2 + hl * 16 : 0;
+                const uint32_t nb = r >= 0 ? 16u : 0u;  // 0: zero-fill, nothing read
+                cp_async16_zfill(st + u * 512, kb + off, nb);
+                cp_async16_zfill(st + u * 512 + 256, vb + off, nb);
+            }
+        };
+#pragma unroll
+        for (int it = 0; it < S - 1; ++it) {
+            if (it < niter) issue(it);
+            cp_async_commit();
+        }
+        for (int it = 0; it < niter; ++it) {
+            if (it + S - 1 < niter) issue(it + S - 1);
+            cp_async_commit();
+            cp_async_wait<S - 1>();
+            const unsigned char* st = ring + size_t(vw) * (S * U * 512) + size_t(it % S) * (U * 512) +
+                                      hl * 16;
+            bool live[U];
+            uint4 kr[U], vr[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = it * kStep + vw * U + u;
+                live[u] = j < cn && ids[j] >= 0;
+                kr[u] = *reinterpret_cast<const uint4*>(st + u * 512);
+                vr[u] = *reinterpret_cast<const uint4*>(st + u * 512 + 256);
+            }
+            float s[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float kf[8];
+                unpack8(kr[u], kf);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(q[h][e], kf[e], acc);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1)
+                        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                    s[u][h] = live[u] ? acc : -CUDART_INF_F;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float mb = s[0][h];
+#pragma unroll
+                for (int u = 1; u < U; ++u) mb = fmaxf(mb, s[u][h]);
+                const float mn = fmaxf(m[h], mb);
+                if (mn == -CUDART_INF_F) continue;  // nothing valid yet
+                const float alpha = exp2f(m[h] - mn);
+                float p[U];
+                float ps = 0.f;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    p[u] = exp2f(s[u][h] - mn);
+                    ps += p[u];
+                }
+                l[h] = l[h] * alpha + ps;
+                m[h] = mn;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float vf[8];
+                    unpack8(vr[u], vf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(p[u], vf[e], o[h][e]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // the ring is reused for the reduction below
+    if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+
+    // Merge the 16 row streams' states (eq. 7) through shared memory.
+    float* so = red;                       // [kVW][G][D]
+    float* sm = red + kVW * G * D;         // [kVW][G]
+    float* sl = sm + kVW * G;              // [kVW][G]
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float4* dst = reinterpret_cast<float4*>(so + (vw * G + h) * D + hl * 8);
+        dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        if (hl == 0) {
+            sm[vw * G + h] = m[h];
+            sl[vw * G + h] = l[h];
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * D; e += kThreads) {
+        const int h = e / D, d = e % D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kVW; ++w)
+            if (sl[w * G + h] > 0.f) M = fmaxf(M, sm[w * G + h]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kVW; ++w) {
+                const float lw = sl[w * G + h];
+                if (!(lw > 0.f)) continue;
+                const float sc = exp2f(sm[w * G + h] - M);
+                L = fmaf(sc, lw, L);
+                O = fmaf(sc, so[(w * G + h) * D + d], O);
+            }
+        }
+        const int64_t qh = int64_t(row) * a.heads + h0 + h;
+        if (a.splits == 1 && !a.force_partial) {
+            a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            if (d == 0 && a.lse != nullptr)
+                a.lse[qh] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+        } else {
+            const int64_t pi = qh * a.part_stride + a.part_base + split;
+            a.part_o[pi * D + d] = O;
+            if (d == 0) {
+                a.part_m[pi] = M;
+                a.part_l[pi] = L;
+            }
+        }
+    }
+}
+
+template <int G, int U, int S>
+int launch_gqa(const AttnArgs& a, int units, hs_stream_t stream) {
+    auto kern = attn_gqa_kernel<G, U, S>;
+    constexpr size_t smem = gqa_smem_bytes<G, U, S>();
+    static int smem_set[64] = {};
+    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem,
+                                                smem_set);
+    if (rc != HS_OK) return rc;
+    dim3 grid(units, a.splits);
+    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return hs_host::launch_status();
 }
 
 template <int DQK, int DV, int G, bool SHARED, int U>
@@ -533,10 +784,10 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         rc = launch<576, 512, 4, true, 2>(a, units, stream);
     } else {
         switch (p.G) {
-            case 1: rc = launch<128, 128, 1, false, 4>(a, units, stream); break;
-            case 2: rc = launch<128, 128, 2, false, 4>(a, units, stream); break;
-            case 4: rc = launch<128, 128, 4, false, 4>(a, units, stream); break;
-            default: rc = launch<128, 128, 8, false, 2>(a, units, stream); break;
+            case 1: rc = launch_gqa<1, 2, 4>(a, units, stream); break;
+            case 2: rc = launch_gqa<2, 2, 4>(a, units, stream); break;
+            case 4: rc = launch_gqa<4, 2, 4>(a, units, stream); break;
+            default: rc = launch_gqa<8, 1, 8>(a, units, stream); break;
         }
     }
     if (rc != HS_OK) return rc;

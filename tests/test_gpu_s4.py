@@ -59,6 +59,26 @@ def test_gqa_small(group):
     assert decode_both(q, k, v, kv_rows, count, 1 / math.sqrt(d), d, kv_heads * d, d) == 0
 
 
+@pytest.mark.parametrize("group", [4, 8])
+def test_gqa_long_lists_one_split(group):
+    """Enough (row, KV head) units that no list is split, each longer than the
+    kernel stages at once (2048 ids): several id chunks per CTA, ragged tail."""
+    rng = np.random.default_rng(70 + group)
+    rows, kv_heads, d, n_kv, cap = 40, 8, 128, 9000, 4500
+    heads = group * kv_heads
+    q = inputs.randn_bf16((rows, heads, d), 71 + group, device="cuda")
+    k = inputs.randn_bf16((n_kv, kv_heads, d), 72 + group, device="cuda")
+    v = inputs.randn_bf16((n_kv, kv_heads, d), 73 + group, device="cuda")
+    kv_rows, count = random_sets(rng, rows, kv_heads, cap, n_kv)
+    count[:4] = cap - np.arange(4)[:, None]
+    for r in range(4):
+        for g in range(kv_heads):
+            kv_rows[r, g] = rng.choice(n_kv, size=cap, replace=False)
+            kv_rows[r, g, count[r, g]:] = -1
+    assert decode_both(q, k, v, kv_rows, count, 1 / math.sqrt(d), d, kv_heads * d, d,
+                       sample_rows=[0, 1, 2, 3, 17, rows - 1]) == 0
+
+
 @pytest.mark.parametrize("heads", [16, 128])
 def test_mla_small(heads):
     rng = np.random.default_rng(heads)
