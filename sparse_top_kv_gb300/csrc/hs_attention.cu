@@ -344,10 +344,10 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     }
     p.chunks_per_kvh = group / p.G;
     const int64_t units = int64_t(rows) * kv_heads * p.chunks_per_kvh;
-    // GQA: one resident wave (two CTAs per SM, one for a group of 8), so that
-    // longer CTAs amortise the Q load, the epilogue and the merge.  MLA on
-    // CUDA cores: up to four CTAs per SM.
-    const int64_t per_sm = p.kind == 2 ? (p.G >= 8 ? 1 : 2) : 4;
+    // GQA: one resident wave (two CTAs per SM), so that longer CTAs amortise
+    // the Q load, the epilogue and the merge.  MLA on CUDA cores: up to four
+    // CTAs per SM.
+    const int64_t per_sm = p.kind == 2 ? 2 : 4;
     const int64_t target = per_sm * hs_host::num_sms();
     int64_t s = hs::max64(1, target / units);
     s = hs::min64(s, std::max(1, cap / 32));
@@ -384,36 +384,76 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// GQA rows of 128 bf16 with K and V in separate caches: a half-warp per
-// candidate row.  Lane l of a half holds d = 8 l .. 8 l + 7 of the row (one
-// 16-byte piece of K and one of V); a (row, head) dot product is 8 FMAs and a
-// 4-step shuffle butterfly inside the half, so every shuffle serves the two
-// rows of a warp.  Each half-warp keeps its own online-softmax state (eqs.
-// 4-6) over its rows; the 16 states of the CTA are merged with eq. (7).
+// Warp-level bf16 tensor-core helpers (mma.sync m16n8k16 and ldmatrix; PTX
+// ISA "Warp-level matrix instructions").  Fragment ownership, g = lane / 4,
+// t = lane % 4: A (16 x 16, row-major) a0 = (g, 2t..2t+1), a1 = (g + 8, 2t..),
+// a2 = (g, 2t + 8..), a3 = (g + 8, 2t + 8..); B (16 x 8, k x n) b0 = (2t..2t+1,
+// g), b1 = (2t + 8.., g); C (16 x 8) c0, c1 = (g, 2t..2t+1), c2, c3 = (g + 8,
+// 2t..).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2,
+                                               uint32_t b0, uint32_t b1) {
+    // Rows 8..15 of A are zero (a head group has at most 8 query heads).
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&d)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&d)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// GQA rows of 128 bf16 with K and V in separate caches, on the warp-level
+// tensor cores.  A head group (G <= 8 query heads of one KV head) is the M
+// dimension of both products, padded to 16: per block of 16 candidates a warp
+// computes S = Q K^T (8 k-steps of 16 dims, two n-tiles of 8 candidates) and
+// O += P V (16 n-tiles of 8 dims, one k-step of 16 candidates), and the S
+// accumulators are the A fragment of P V in place, so the online softmax
+// (eqs. 4-6, exp2 domain) runs on registers between the two: four scores a
+// lane, two shuffles for the row maximum, and the row sum kept per lane until
+// the end.  The contraction is only G wide, so the kernel is HBM-bound; the
+// tensor cores are there to take the dot products off the issue slots.
 //
 // Loads: the CTA's candidate ids are staged in shared memory (one coalesced
-// read per chunk of kIdChunk), and every lane streams its own 16-byte pieces
-// of K and V through a private S-stage cp.async ring in shared memory, so
-// S - 1 iterations of U rows per half-warp are in flight while one is
-// computed.  A lane reads back only what it copied itself: the cp.async
-// group wait of the thread is the only synchronisation the ring needs.
+// read per chunk of kIdChunk); each warp streams its blocks (every W-th block
+// of 16) through a private S-stage cp.async ring of [16 x 256 B] K and V tiles
+// whose 16-byte chunks are XOR-swizzled by (candidate mod 8), so that every
+// 8 x 8 ldmatrix touches 8 distinct bank groups.  Absent candidates are zero-
+// filled and masked.  Each warp keeps its own state; the W states are merged
+// with eq. (7) through shared memory, the splits by merge_kernel.
 constexpr int kIdChunk = 2048;
+constexpr int kGqaBlock = 16;                 // candidates per warp step
+constexpr int kGqaTile = kGqaBlock * 256;     // bytes of one K (or V) tile
 
-template <int G, int U, int S>
+template <int G, int W, int S>
 constexpr size_t gqa_smem_bytes() {
-    constexpr size_t ring = size_t(kWarps) * 2 * S * U * 2 * 256;
-    constexpr size_t reduce = size_t(kWarps) * 2 * G * (128 + 2) * sizeof(float);
+    constexpr size_t ring = size_t(W) * S * 2 * kGqaTile;
+    constexpr size_t reduce = size_t(W) * G * (128 + 2) * sizeof(float);
     return kIdChunk * sizeof(int32_t) + (ring > reduce ? ring : reduce);
 }
 
-template <int G, int U, int S>
-__global__ void __launch_bounds__(kThreads, G >= 8 ? 1 : 2) attn_gqa_kernel(const AttnArgs a) {
+template <int G, int W, int S>
+__global__ void __launch_bounds__(W * 32) attn_gqa_kernel(const AttnArgs a) {
+    static_assert(G >= 1 && G <= 8, "a head group fills at most half of the MMA rows");
     constexpr int D = 128;
-    constexpr int kVW = kWarps * 2;               // row streams (half-warps) per CTA
-    extern __shared__ __align__(16) unsigned char gsm[];
+    extern __shared__ __align__(128) unsigned char gsm[];
     int32_t* ids = reinterpret_cast<int32_t*>(gsm);                    // [kIdChunk]
-    unsigned char* ring = gsm + kIdChunk * sizeof(int32_t);            // [kVW][S][U][K,V][256 B]
-    float* red = reinterpret_cast<float*>(ring);  // after the loop: [kVW][G][D] + m, l [kVW][G]
+    unsigned char* ring = gsm + kIdChunk * sizeof(int32_t);            // [W][S][K, V tile]
+    float* red = reinterpret_cast<float*>(ring);  // after the loop: [W][G][D] + m, l [W][G]
 
     const int unit = blockIdx.x;
     const int split = blockIdx.y;
@@ -423,36 +463,23 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 1 : 2) attn_gqa_kernel(cons
     const int group = a.heads / a.kv_heads;
     const int h0 = kvh * group + chunk * G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hl = lane & 15;                     // lane within the half-warp
-    const int vw = warp * 2 + (lane >> 4);        // row stream of this half-warp
+    const int g = lane >> 2, t = lane & 3;
 
-    auto unpack8 = [](const uint4& u, float (&f)[8]) {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    // Q as the A fragment of 8 k-steps (rows g < G; the other rows are 0).
+    uint32_t qa[8][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            a.q + (int64_t(row) * a.heads + h0 + min(g, G - 1)) * D);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        for (int ks = 0; ks < 8; ++ks) {
+            qa[ks][0] = g < G ? __ldg(qrow + ks * 8 + t) : 0u;
+            qa[ks][1] = g < G ? __ldg(qrow + ks * 8 + 4 + t) : 0u;
         }
-    };
-    // Query slice, pre-scaled into the exp2 domain.
-    float q[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                                    a.q + (int64_t(row) * a.heads + h0 + h) * D) + hl);
-        unpack8(raw, q[h]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) q[h][e] *= a.scale_log2;
     }
-    float o[G][8];
-    float m[G], l[G];
+    float o[16][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = -CUDART_INF_F;
-        l[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
-    }
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m = -CUDART_INF_F, l = 0.f;  // state of head row g (l: this lane's columns)
 
     const int64_t idx_base = (int64_t(row) * a.kv_heads + kvh) * a.cap;
     const int n = a.count ? min(max(a.count[int64_t(row) * a.kv_heads + kvh], 0), a.cap) : a.cap;
@@ -460,34 +487,39 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 1 : 2) attn_gqa_kernel(cons
     const int t0 = min(n, split * per), t1 = min(n, t0 + per);
     const char* kb = reinterpret_cast<const char*>(a.k) + int64_t(kvh) * a.head_stride * 2;
     const char* vb = reinterpret_cast<const char*>(a.v) + int64_t(kvh) * a.head_stride * 2;
-    const uint32_t ring_me = hs::smem_u32(ring) + uint32_t(vw) * (S * U * 512) + hl * 16;
-    constexpr int kStep = kVW * U;                // rows per CTA iteration
+    const uint32_t ring_w = hs::smem_u32(ring) + uint32_t(warp) * (S * 2 * kGqaTile);
     bool bad = false;
 
-    // A staged id is the cache row, or -1 when the candidate is not live
-    // (padding, or out of the cache's range: flagged, contributes nothing).
+    // Copy lanes: 16-byte chunk cc = lane % 16 of candidates 2 i + lane / 16,
+    // i = 0..7, so that one warp-wide copy moves two whole rows.
+    const int cc = lane & 15, ch = lane >> 4;
+    // ldmatrix lanes: matrix mi = lane / 8, row r = lane % 8 of it.
+    const int mi = lane >> 3, r8 = lane & 7;
+
     for (int c0 = t0; c0 < t1; c0 += kIdChunk) {
         const int cn = min(kIdChunk, t1 - c0);
         __syncthreads();  // the previous chunk's ids are no longer read
-        for (int i = threadIdx.x; i < cn; i += kThreads) {
+        for (int i = threadIdx.x; i < cn; i += W * 32) {
             const int32_t r = __ldg(a.kv_rows + idx_base + c0 + i);
             if (r >= a.num_kv_rows) bad = true;
             ids[i] = r < a.num_kv_rows ? r : -1;
         }
         __syncthreads();
-        // Both halves of a warp run the same number of iterations (the dot
-        // products shuffle across the whole warp); rows past cn are not live.
-        const int niter = (cn + kStep - 1) / kStep;
+        const int nblk = (cn + kGqaBlock - 1) / kGqaBlock;
+        const int niter = nblk > warp ? (nblk - warp + W - 1) / W : 0;  // warp-uniform
         auto issue = [&](int it) {
-            const uint32_t st = ring_me + uint32_t(it % S) * (U * 512);
+            const int jb = (it * W + warp) * kGqaBlock;
+            const uint32_t st = ring_w + uint32_t(it % S) * (2 * kGqaTile);
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = it * kStep + vw * U + u;
+            for (int i = 0; i < kGqaBlock / 2; ++i) {
+                const int key = 2 * i + ch;
+                const int j = jb + key;
                 const int32_t r = j < cn ? ids[j] : -1;
-                const int64_t off = r >= 0 ? int64_t(r) * a.row_stride * 2 + hl * 16 : 0;
+                const int64_t off = r >= 0 ? int64_t(r) * a.row_stride * 2 + cc * 16 : 0;
                 const uint32_t nb = r >= 0 ? 16u : 0u;  // 0: zero-fill, nothing read
-                cp_async16_zfill(st + u * 512, kb + off, nb);
-                cp_async16_zfill(st + u * 512 + 256, vb + off, nb);
+                const uint32_t dst = st + key * 256 + uint32_t((cc ^ (key & 7)) * 16);
+                cp_async16_zfill(dst, kb + off, nb);
+                cp_async16_zfill(dst + kGqaTile, vb + off, nb);
             }
         };
 #pragma unroll
@@ -499,91 +531,102 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 1 : 2) attn_gqa_kernel(cons
             if (it + S - 1 < niter) issue(it + S - 1);
             cp_async_commit();
             cp_async_wait<S - 1>();
-            const unsigned char* st = ring + size_t(vw) * (S * U * 512) + size_t(it % S) * (U * 512) +
-                                      hl * 16;
-            bool live[U];
-            uint4 kr[U], vr[U];
+            __syncwarp();
+            const uint32_t kt = ring_w + uint32_t(it % S) * (2 * kGqaTile);
+            const uint32_t vt = kt + kGqaTile;
+
+            // S = Q K^T: n-tile 0 = candidates 0..7, n-tile 1 = 8..15.
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int key = r8 + (mi >> 1) * 8;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = it * kStep + vw * U + u;
-                live[u] = j < cn && ids[j] >= 0;
-                kr[u] = *reinterpret_cast<const uint4*>(st + u * 512);
-                vr[u] = *reinterpret_cast<const uint4*>(st + u * 512 + 256);
-            }
-            float s[U][G];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float kf[8];
-                unpack8(kr[u], kf);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(q[h][e], kf[e], acc);
-#pragma unroll
-                    for (int off = 8; off > 0; off >>= 1)
-                        acc += __shfl_xor_sync(0xffffffffu, acc, off);
-                    s[u][h] = live[u] ? acc : -CUDART_INF_F;
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int c = 2 * ks + (mi & 1);
+                    uint32_t b[4];
+                    ldsm_x4(kt + key * 256 + ((c ^ r8) * 16), b);
+                    mma_bf16_16816(s0, qa[ks][0], qa[ks][1], b[0], b[1]);
+                    mma_bf16_16816(s1, qa[ks][0], qa[ks][1], b[2], b[3]);
                 }
             }
+            // Online softmax of head row g over this lane's four candidates.
+            const int jb = (it * W + warp) * kGqaBlock;
+            float x[4] = {s0[0], s0[1], s1[0], s1[1]};
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float mb = s[0][h];
+            for (int i = 0; i < 4; ++i) {
+                const int j = jb + (i >> 1) * 8 + 2 * t + (i & 1);
+                const bool live = j < cn && ids[j] >= 0;
+                x[i] = live ? x[i] * a.scale_log2 : -CUDART_INF_F;
+            }
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mn = fmaxf(m, mx);
+            float alpha = 1.f;
+            uint32_t pa0 = 0u, pa2 = 0u;
+            if (mn != -CUDART_INF_F) {
+                alpha = exp2f(m - mn);
+                // P is rounded to bf16 for the MMA; the row sum uses the
+                // rounded weights so that numerator and denominator agree.
+                pa0 = pack_bf16x2(exp2f(x[0] - mn), exp2f(x[1] - mn));
+                pa2 = pack_bf16x2(exp2f(x[2] - mn), exp2f(x[3] - mn));
+                const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa0));
+                const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa2));
+                l = l * alpha + ((p01.x + p01.y) + (p23.x + p23.y));
+                m = mn;
+            }
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                for (int u = 1; u < U; ++u) mb = fmaxf(mb, s[u][h]);
-                const float mn = fmaxf(m[h], mb);
-                if (mn == -CUDART_INF_F) continue;  // nothing valid yet
-                const float alpha = exp2f(m[h] - mn);
-                float p[U];
-                float ps = 0.f;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    p[u] = exp2f(s[u][h] - mn);
-                    ps += p[u];
-                }
-                l[h] = l[h] * alpha + ps;
-                m[h] = mn;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    float vf[8];
-                    unpack8(vr[u], vf);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(p[u], vf[e], o[h][e]);
+                for (int nt = 0; nt < 16; ++nt) {
+                    o[nt][0] *= alpha;
+                    o[nt][1] *= alpha;
                 }
             }
+            // O += P V: n-tiles 2 np and 2 np + 1 (dims 16 np .. 16 np + 15).
+            {
+                const int key = r8 + (mi & 1) * 8;
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    const int c = 2 * np + (mi >> 1);
+                    uint32_t b[4];
+                    ldsm_x4_trans(vt + key * 256 + ((c ^ r8) * 16), b);
+                    mma_bf16_16816(o[2 * np], pa0, pa2, b[0], b[1]);
+                    mma_bf16_16816(o[2 * np + 1], pa0, pa2, b[2], b[3]);
+                }
+            }
+            __syncwarp();  // every lane's reads of this stage precede its refill
         }
     }
     cp_async_wait<0>();
-    __syncthreads();  // the ring is reused for the reduction below
     if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    __syncthreads();  // the ring is reused for the reduction below
 
-    // Merge the 16 row streams' states (eq. 7) through shared memory.
-    float* so = red;                       // [kVW][G][D]
-    float* sm = red + kVW * G * D;         // [kVW][G]
-    float* sl = sm + kVW * G;              // [kVW][G]
+    // Merge the W warps' states (eq. 7) through shared memory.
+    float* so = red;                     // [W][G][D]
+    float* sm = red + W * G * D;         // [W][G]
+    float* sl = sm + W * G;              // [W][G]
+    if (g < G) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float4* dst = reinterpret_cast<float4*>(so + (vw * G + h) * D + hl * 8);
-        dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-        dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
-        if (hl == 0) {
-            sm[vw * G + h] = m[h];
-            sl[vw * G + h] = l[h];
+        for (int nt = 0; nt < 16; ++nt)
+            *reinterpret_cast<float2*>(so + (warp * G + g) * D + nt * 8 + 2 * t) =
+                make_float2(o[nt][0], o[nt][1]);
+        if (t == 0) {
+            sm[warp * G + g] = m;
+            sl[warp * G + g] = l;
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * D; e += kThreads) {
+    for (int e = threadIdx.x; e < G * D; e += W * 32) {
         const int h = e / D, d = e % D;
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < kVW; ++w)
+        for (int w = 0; w < W; ++w)
             if (sl[w * G + h] > 0.f) M = fmaxf(M, sm[w * G + h]);
         float L = 0.f, O = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
-            for (int w = 0; w < kVW; ++w) {
+            for (int w = 0; w < W; ++w) {
                 const float lw = sl[w * G + h];
                 if (!(lw > 0.f)) continue;
                 const float sc = exp2f(sm[w * G + h] - M);
@@ -607,16 +650,21 @@ __global__ void __launch_bounds__(kThreads, G >= 8 ? 1 : 2) attn_gqa_kernel(cons
     }
 }
 
-template <int G, int U, int S>
+// Warps per CTA and ring stages of the GQA kernel: two CTAs per SM (about
+// 104 KB of shared memory each), 2 x 4 warps x 2 blocks of 8 KB in flight.
+constexpr int kGqaWarps = 4;
+constexpr int kGqaStages = 3;
+
+template <int G>
 int launch_gqa(const AttnArgs& a, int units, hs_stream_t stream) {
-    auto kern = attn_gqa_kernel<G, U, S>;
-    constexpr size_t smem = gqa_smem_bytes<G, U, S>();
+    auto kern = attn_gqa_kernel<G, kGqaWarps, kGqaStages>;
+    constexpr size_t smem = gqa_smem_bytes<G, kGqaWarps, kGqaStages>();
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem,
                                                 smem_set);
     if (rc != HS_OK) return rc;
     dim3 grid(units, a.splits);
-    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    kern<<<grid, kGqaWarps * 32, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return hs_host::launch_status();
 }
 
@@ -784,10 +832,10 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         rc = launch<576, 512, 4, true, 2>(a, units, stream);
     } else {
         switch (p.G) {
-            case 1: rc = launch_gqa<1, 2, 4>(a, units, stream); break;
-            case 2: rc = launch_gqa<2, 2, 4>(a, units, stream); break;
-            case 4: rc = launch_gqa<4, 2, 4>(a, units, stream); break;
-            default: rc = launch_gqa<8, 1, 8>(a, units, stream); break;
+            case 1: rc = launch_gqa<1>(a, units, stream); break;
+            case 2: rc = launch_gqa<2>(a, units, stream); break;
+            case 4: rc = launch_gqa<4>(a, units, stream); break;
+            default: rc = launch_gqa<8>(a, units, stream); break;
         }
     }
     if (rc != HS_OK) return rc;
