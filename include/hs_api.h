@@ -209,11 +209,10 @@ int hs_backup(const void* src, const int64_t* src_rows, void* host_pool,
  *            round to nearest even).
  * lse        fp32 [rows, heads] natural-log LSE, or NULL.
  * workspace  device scratch of at least hs_sparse_decode_workspace_bytes(..)
- *            bytes (split-KV partial states; for the MLA tensor-core kernel
- *            also one arrival counter per (row, head group), zeroed by the
- *            call, so that the split that finishes last merges the others in
- *            its epilogue instead of a second launch); may be NULL when that
- *            is 0.
+ *            bytes (split-KV partial states, and one arrival counter per
+ *            (row, kv head, head group), zeroed by the call, so that the
+ *            split that finishes last merges the others in its epilogue
+ *            instead of a second launch); may be NULL when that is 0.
  * status     int32 device word or NULL (HS_ERR_TIMEOUT from bounded waits,
  *            HS_ERR_BAD_INDEX from skipped rows).
  * Supported shapes: (d_qk, d_v) = (576, 512) with kv_heads == 1 and k_base

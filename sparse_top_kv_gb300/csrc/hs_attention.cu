@@ -50,6 +50,7 @@ struct AttnArgs {
     int32_t splits, chunks_per_kvh;
     int32_t* status;
     int32_t part_stride, part_base, force_partial;
+    int32_t* sync;  // GQA: one arrival counter per unit (zeroed), the last split merges; or null
 };
 
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
@@ -313,10 +314,11 @@ struct Plan {
     int G;     // heads per CTA
     int chunks_per_kvh;
     int splits;
+    int kv_heads;
 };
 
 Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bool shared) {
-    Plan p{0, 0, 0, 1};
+    Plan p{0, 0, 0, 1, kv_heads};
     if (rows <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads) return p;
     const int group = heads / kv_heads;
     const bool mla = d_qk == 576 && d_v == 512 && kv_heads == 1 && shared;
@@ -344,10 +346,10 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     }
     p.chunks_per_kvh = group / p.G;
     const int64_t units = int64_t(rows) * kv_heads * p.chunks_per_kvh;
-    // GQA: one resident wave (two CTAs per SM), so that longer CTAs amortise
+    // GQA: one resident wave (one CTA per SM), so that longer CTAs amortise
     // the Q load, the epilogue and the merge.  MLA on CUDA cores: up to four
     // CTAs per SM.
-    const int64_t per_sm = p.kind == 2 ? 2 : 4;
+    const int64_t per_sm = p.kind == 2 ? 1 : 4;
     const int64_t target = per_sm * hs_host::num_sms();
     int64_t s = hs::max64(1, target / units);
     s = hs::min64(s, std::max(1, cap / 32));
@@ -356,19 +358,21 @@ Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bo
     return p;
 }
 
-// Bytes of the partial states; the tcgen05 kernel also keeps one arrival
-// counter per (row, head group) behind them, 16-byte aligned.
+// Bytes of the partial states; the tcgen05 MLA and the GQA kernels also keep
+// one arrival counter per work unit behind them, 16-byte aligned.
 int64_t partial_bytes(const Plan& p, int rows, int heads, int d_v) {
     const int64_t n = int64_t(rows) * heads;
     return n * p.splits * (2 + int64_t(d_v)) * int64_t(sizeof(float));
 }
 
-int64_t sync_words(const Plan& p, int rows) { return int64_t(rows) * p.chunks_per_kvh; }
+int64_t sync_words(const Plan& p, int rows) {
+    return int64_t(rows) * p.kv_heads * p.chunks_per_kvh;
+}
 
 int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
     if (p.kind == 0 || p.splits <= 1) return 0;
     int64_t b = partial_bytes(p, rows, heads, d_v);
-    if (p.kind == 3) b += (sync_words(p, rows) * 4 + 15) / 16 * 16;
+    if (p.kind == 3 || p.kind == 2) b += (sync_words(p, rows) * 4 + 15) / 16 * 16;
     return b;
 }
 
@@ -436,6 +440,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // filled and masked.  Each warp keeps its own state; the W states are merged
 // with eq. (7) through shared memory, the splits by merge_kernel.
 constexpr int kIdChunk = 2048;
+constexpr int kGqaMaxSplits = 64;             // splits of one unit (the plan's limit)
 constexpr int kGqaBlock = 16;                 // candidates per warp step
 constexpr int kGqaTile = kGqaBlock * 256;     // bytes of one K (or V) tile
 
@@ -648,11 +653,62 @@ __global__ void __launch_bounds__(W * 32) attn_gqa_kernel(const AttnArgs a) {
             }
         }
     }
+    if (a.sync == nullptr) return;
+
+    // Split merge (eq. 7) by the split of this unit that finishes last: every
+    // split publishes its partial state, then counts itself in; the one that
+    // sees splits - 1 earlier arrivals reads all of them back from L2, in
+    // three dependent steps: the (m, l) pairs into shared memory, the weights
+    // of each head, then the partial outputs with independent loads.
+    __shared__ int last_split;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_split = atomicAdd(a.sync + unit, 1) == a.splits - 1;
+    __syncthreads();
+    if (!last_split) return;
+    __threadfence();
+    float* wm = red;                              // [G][kGqaMaxSplits] m, then weights
+    float* wl = red + G * kGqaMaxSplits;          // [G][kGqaMaxSplits] l
+    float* winv = wl + G * kGqaMaxSplits;         // [G] 1 / L and [G] lse
+    const int64_t qh0 = int64_t(row) * a.heads + h0;
+    for (int e = threadIdx.x; e < G * a.splits; e += W * 32) {
+        const int h = e / a.splits, sp = e % a.splits;
+        wm[h * kGqaMaxSplits + sp] = __ldcg(a.part_m + (qh0 + h) * a.part_stride + sp);
+        wl[h * kGqaMaxSplits + sp] = __ldcg(a.part_l + (qh0 + h) * a.part_stride + sp);
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {
+        const int h = threadIdx.x;
+        float M = -CUDART_INF_F;
+        for (int sp = 0; sp < a.splits; ++sp)
+            if (wl[h * kGqaMaxSplits + sp] > 0.f) M = fmaxf(M, wm[h * kGqaMaxSplits + sp]);
+        float L = 0.f;
+        for (int sp = 0; sp < a.splits; ++sp) {
+            const float lw = wl[h * kGqaMaxSplits + sp];
+            const float sc = (M != -CUDART_INF_F && lw > 0.f)
+                                 ? exp2f(wm[h * kGqaMaxSplits + sp] - M) : 0.f;
+            L = fmaf(sc, lw, L);
+            wm[h * kGqaMaxSplits + sp] = sc;
+        }
+        winv[h] = L > 0.f ? 1.f / L : 0.f;
+        winv[G + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * D; e += W * 32) {
+        const int h = e / D, d = e % D;
+        const float* po = a.part_o + (qh0 + h) * a.part_stride * D + d;
+        float O = 0.f;
+#pragma unroll 8
+        for (int sp = 0; sp < a.splits; ++sp)
+            O = fmaf(wm[h * kGqaMaxSplits + sp], __ldcg(po + int64_t(sp) * D), O);
+        a.out[(qh0 + h) * D + d] = __float2bfloat16_rn(O * winv[h]);
+        if (d == 0 && a.lse != nullptr) a.lse[qh0 + h] = winv[G + h];
+    }
 }
 
-// Warps per CTA and ring stages of the GQA kernel: two CTAs per SM (about
-// 104 KB of shared memory each), 2 x 4 warps x 2 blocks of 8 KB in flight.
-constexpr int kGqaWarps = 4;
+// Warps per CTA and ring stages of the GQA kernel: one CTA per SM (about
+// 200 KB of shared memory), 8 warps x 2 blocks of 8 KB in flight.
+constexpr int kGqaWarps = 8;
 constexpr int kGqaStages = 3;
 
 template <int G>
@@ -765,7 +821,7 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
             a.part_m = w;
             a.part_l = w + n * p.splits;
             a.part_o = w + 2 * n * p.splits;
-            if (p.kind == 3 && p.splits <= kMlaMaxMerge && al(a.part_o)) {
+            if ((p.kind == 3 && p.splits <= kMlaMaxMerge && al(a.part_o)) || p.kind == 2) {
                 sync = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
                                                   partial_bytes(p, rows, heads, d_v));
                 merge_total = p.splits;
@@ -796,6 +852,11 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
     a.chunks_per_kvh = p.chunks_per_kvh;
     a.status = status;
     const int units = rows * kv_heads * p.chunks_per_kvh;
+    a.sync = sync;
+    if (sync != nullptr &&
+        cudaMemsetAsync(sync, 0, size_t(units) * sizeof(int32_t),
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return HS_ERR_CUDA;
     int rc;
     if (p.kind == 3) {
         MlaArgs m{};
@@ -823,10 +884,6 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         m.merge_total = merge_total;
         m.status = status;
         m.timeout_ns = hs::kWaitTimeoutNs;
-        if (sync != nullptr &&
-            cudaMemsetAsync(sync, 0, size_t(units) * sizeof(int32_t),
-                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-            return HS_ERR_CUDA;
         rc = launch_mla_tc(m, p.G, dim3(units, pl.splits), stream);
     } else if (p.kind == 1) {
         rc = launch<576, 512, 4, true, 2>(a, units, stream);
