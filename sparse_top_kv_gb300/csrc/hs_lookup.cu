@@ -5,7 +5,8 @@
 // invalidated before reuse).
 //
 // GB300 design: one 1024-thread CTA per request row.  Phase 1 builds an
-// open-addressing hash of the row's pending slot ids in shared memory; the
+// open-addressing hash (4-slot buckets, load <= 1/4 where shared memory
+// allows, else <= 1/2) of the row's pending slot ids in shared memory; the
 // first occurrence of a repeated id is kept with atomicMin on its position,
 // so repeats resolve deterministically (the walkthrough's hash overwrites on
 // a repeated key, which is racy).  Phase 2 walks the LRU list with each
@@ -13,8 +14,11 @@
 // memory); hits and evictables are compacted in LRU order by one block-wide
 // shuffle scan.  Phase 3 ranks the misses in row order with the same scan and
 // hands them E[0], E[1], ...  Phase 4 writes
-// E[M:] ++ E[:M] ++ hits.  The output is bit-identical to the sequential
-// definition for every thread schedule.
+// E[M:] ++ E[:M] ++ hits.  Every global read is issued in one batch at the
+// start, and the per-entry outputs are kept in shared memory until one
+// coalesced pass at the end (hits land at random entries: storing them from
+// the walk would cost one L1 wavefront per hit).  The output is bit-
+// identical to the sequential definition for every thread schedule.
 #include "hs_common.cuh"
 
 namespace {
@@ -22,6 +26,7 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int32_t kEmpty = -1;
 constexpr int32_t kDone = INT32_MIN;
+constexpr uint8_t kNone = 0, kHit = 1, kMiss = 2;
 constexpr int kMaxSmem = 227 * 1024;
 
 struct LookupArgs {
@@ -49,17 +54,39 @@ __device__ __forceinline__ uint32_t hash_of(int32_t g, int log2n) {
     return (uint32_t(g) * 2654435761u) >> (32 - log2n);
 }
 
+// The hash is linear probing over aligned buckets of 4 slots: a key's probe
+// sequence starts at the first slot of its bucket, so a lookup reads one
+// bucket per 16-byte load, and at a load factor <= 1/4 almost every lookup
+// ends in its first bucket (a warp then runs no divergent probe loop).
 // Position of key g in the table, or -1 when absent.
 __device__ __forceinline__ int find_key(const int32_t* keys, int32_t g, int log2n) {
     const uint32_t mask = (1u << log2n) - 1u;
-    uint32_t h = hash_of(g, log2n);
-    for (uint32_t probe = 0; probe <= mask; ++probe) {
-        const int32_t k = keys[h];
-        if (k == g) return int(h);
-        if (k == kEmpty) return -1;
-        h = (h + 1u) & mask;
+    uint32_t b = hash_of(g, log2n) & ~3u;
+    for (uint32_t probe = 0; probe <= mask; probe += 4) {
+        const int4 k = *reinterpret_cast<const int4*>(keys + b);
+        if (k.x == g) return int(b);
+        if (k.x == kEmpty) return -1;
+        if (k.y == g) return int(b + 1);
+        if (k.y == kEmpty) return -1;
+        if (k.z == g) return int(b + 2);
+        if (k.z == kEmpty) return -1;
+        if (k.w == g) return int(b + 3);
+        if (k.w == kEmpty) return -1;
+        b = (b + 4u) & mask;
     }
     return -1;
+}
+
+// Slot of key g, inserting it at the first empty slot of its probe sequence.
+__device__ __forceinline__ int insert_key(int32_t* keys, int32_t g, int log2n) {
+    const uint32_t mask = (1u << log2n) - 1u;
+    uint32_t h = hash_of(g, log2n) & ~3u;
+    for (uint32_t probe = 0; probe <= mask; ++probe) {
+        const int32_t old = atomicCAS(&keys[h], kEmpty, g);
+        if (old == kEmpty || old == g) return int(h);
+        h = (h + 1u) & mask;
+    }
+    return -1;  // unreachable: the table holds at least 4x the keys
 }
 
 __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
@@ -72,11 +99,13 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     const int hot_size = a.hot_size;
     int32_t* keys = reinterpret_cast<int32_t*>(smem);
     int32_t* vals = keys + HS;
-    int32_t* state = vals + HS;
-    int32_t* s_dgi = state + cap;
+    int32_t* state = vals + HS;       // pending id, or kDone
+    int32_t* outv = state + cap;      // hot_idx value of each entry
+    int32_t* s_dgi = outv + cap;
     int16_t* s_lru = reinterpret_cast<int16_t*>(s_dgi + hot_size);
     int16_t* E = s_lru + hot_size;
     int16_t* H = E + hot_size;
+    uint8_t* kind = reinterpret_cast<uint8_t*>(H + hot_size);  // kNone / kHit / kMiss
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
@@ -107,47 +136,36 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     int16_t* lru = a.lru + int64_t(row) * hot_size;
     const int64_t hot_base = int64_t(row) * a.region_stride;
 
-    // Stage the row's state (coalesced) and clear the hash.
+    // Every global read of the kernel is issued here, in one batch: the
+    // row's state, its pending ids and its count; the hash is cleared.
+    const int n = a.count ? min(max(a.count[row], 0), cap) : cap;
+    const int32_t newest = a.newest_slot ? a.newest_slot[row] : -1;
     for (int j = tid; j < hot_size; j += kThreads) {
         s_dgi[j] = dgi[j];
         s_lru[j] = lru[j];
     }
-    for (int h = tid; h < HS; h += kThreads) {
-        keys[h] = kEmpty;
-        vals[h] = INT32_MAX;
+    for (int i = tid; i < cap; i += kThreads) state[i] = g_row[i];
+    for (int h = tid * 4; h < HS; h += kThreads * 4) {
+        *reinterpret_cast<int4*>(keys + h) = make_int4(kEmpty, kEmpty, kEmpty, kEmpty);
+        *reinterpret_cast<int4*>(vals + h) = make_int4(INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX);
     }
     if (tid == 0) s_dup = 0;
     __syncthreads();
 
-    const int n = a.count ? min(max(a.count[row], 0), cap) : cap;
-    const int32_t newest = a.newest_slot ? a.newest_slot[row] : -1;
-
     // Phase 1: classify entries, hash the pending ids (first occurrence wins).
-    const uint32_t hmask = uint32_t(HS) - 1u;
     for (int i = tid; i < cap; i += kThreads) {
-        const int32_t g = i < n ? g_row[i] : -1;
-        if (mm) mm[i] = 0;
-        msrc[i] = -1;
-        mdst[i] = -1;
-        if (mrow) mrow[i] = -1;
+        const int32_t g = i < n ? state[i] : -1;
         if (g < 0) {
-            out[i] = -1;
-            if (hidx) hidx[i] = -1;
+            outv[i] = -1;
+            kind[i] = kNone;
             state[i] = kDone;
         } else if (newest >= 0 && g == newest) {
-            out[i] = int32_t(hot_base + hot_size);
-            if (hidx) hidx[i] = int32_t(hot_base + hot_size);
+            outv[i] = int32_t(hot_base + hot_size);
+            kind[i] = kHit;
             state[i] = kDone;
         } else {
-            uint32_t h = hash_of(g, a.hash_log2);
-            for (uint32_t probe = 0; probe <= hmask; ++probe) {
-                const int32_t old = atomicCAS(&keys[h], kEmpty, g);
-                if (old == kEmpty || old == g) {
-                    atomicMin(&vals[h], i);
-                    break;
-                }
-                h = (h + 1u) & hmask;
-            }
+            const int h = insert_key(keys, g, a.hash_log2);
+            if (h >= 0) atomicMin(&vals[h], i);
             state[i] = g;
         }
     }
@@ -161,8 +179,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
             const int h = find_key(keys, g, a.hash_log2);
             if (h >= 0 && vals[h] != i) {
                 state[i] = kDone;
-                out[i] = -1;
-                if (hidx) hidx[i] = -1;
+                outv[i] = -1;
+                kind[i] = kNone;
                 ++dups;
             }
         }
@@ -172,7 +190,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
 
     // Phase 2: LRU walk, least -> most recently used.  Thread t owns the
     // contiguous positions [t*K2, t*K2 + K2); one block scan orders hits and
-    // evictables exactly as a sequential walk would.
+    // evictables exactly as a sequential walk would.  Results stay in shared
+    // memory; the global outputs are written once, coalesced, at the end.
     const int K2 = (hot_size + kThreads - 1) / kThreads;  // <= 32
     uint32_t hitmask = 0;
     int nh = 0;
@@ -187,8 +206,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         const int h = find_key(keys, cg, a.hash_log2);
         if (h < 0) continue;
         const int i = vals[h];
-        out[i] = int32_t(hot_base + sl);
-        if (hidx) hidx[i] = int32_t(hot_base + sl);
+        outv[i] = int32_t(hot_base + sl);
+        kind[i] = kHit;
         state[i] = kDone;
         hitmask |= 1u << k;
         ++nh;
@@ -225,20 +244,41 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         const int32_t g = state[i];
         if (g == kDone) continue;
         const int16_t sl = m < nE ? E[m] : int16_t(-1);
-        if (hidx) hidx[i] = -1;
         if (sl >= 0 && sl < hot_size) {
-            out[i] = int32_t(hot_base + sl);
-            if (mm) mm[i] = 1;
+            outv[i] = int32_t(hot_base + sl);
+            kind[i] = kMiss;
             dgi[sl] = g;
             msrc[m] = g;
             mdst[m] = hot_base + sl;
             if (mrow) mrow[m] = int32_t(hot_base + sl);
         } else {
-            out[i] = -1;  // only reachable with a corrupted LRU list
+            outv[i] = -1;  // only reachable with a corrupted LRU list
+            kind[i] = kNone;
+            if (m < nE) {
+                msrc[m] = -1;
+                mdst[m] = -1;
+                if (mrow) mrow[m] = -1;
+            }
         }
         ++m;
     }
     const int M = min(miss_total, nE);
+    __syncthreads();
+
+    // Outputs, coalesced: hot_idx, hit_idx, miss_mask of every entry, and the
+    // unused tails of the miss lists.
+    for (int i = tid; i < cap; i += kThreads) {
+        const int32_t v = outv[i];
+        const uint8_t kd = kind[i];
+        out[i] = v;
+        if (hidx) hidx[i] = kd == kHit ? v : -1;
+        if (mm) mm[i] = kd == kMiss ? 1 : 0;
+        if (i >= M) {
+            msrc[i] = -1;
+            mdst[i] = -1;
+            if (mrow) mrow[i] = -1;
+        }
+    }
 
     // Phase 4: new LRU order = E[M:] ++ E[:M] ++ hits.
     for (int j = tid; j < hot_size; j += kThreads) {
@@ -294,10 +334,14 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
         (cap > 0 && (hot_idx == nullptr || miss_src == nullptr || miss_dst == nullptr)) ||
         miss_count == nullptr || stats == nullptr || err == nullptr)
         return HS_ERR_INVALID_ARG;
+    // Hash of load factor <= 1/4, or <= 1/2 when the larger table does not fit.
+    const auto smem_for = [&](int l2) {
+        return size_t(8) * (size_t(1) << l2) + size_t(9) * cap + size_t(10) * hot_size;
+    };
     int log2n = 6;
-    while ((1 << log2n) < 2 * cap) ++log2n;
-    const size_t smem = size_t(8) * (size_t(1) << log2n) + size_t(4) * cap +
-                        size_t(10) * hot_size;
+    while ((1 << log2n) < 4 * cap) ++log2n;
+    if (smem_for(log2n) > size_t(kMaxSmem) && log2n > 6) --log2n;
+    const size_t smem = smem_for(log2n);
     if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(lookup_kernel),
