@@ -340,6 +340,25 @@ def bench_swapin(reps=10):
         b.synchronize()
         if i >= 3:
             times.append(a.elapsed_time(b))
+    # The two halves alone (64-row runs; scattered rows, the step's pattern),
+    # on every SM and on the step's SM budget for the copy.
+    half = torch.arange(R, device="cuda") < R // 2
+    parts = {}
+    for name, sel in (("runs", half), ("scattered", ~half)):
+        cnt = torch.where(sel, M, 0).to(torch.int32)
+        for ctas in (0, 24):
+            tt = []
+            for i in range(reps + 3):
+                a, b = ev(), ev()
+                a.record()
+                hs.swap_in(pdev, pool.shape[0], hot, ROW_BYTES, msrc, mdst, cnt,
+                           max_ctas=ctas, status=status)
+                b.record()
+                b.synchronize()
+                if i >= 3:
+                    tt.append(a.elapsed_time(b))
+            key = f"{name}_gbs" + ("" if ctas == 0 else f"_{ctas}sm")
+            parts[key] = (R // 2) * M * ROW_BYTES / statistics.median(tt) / 1e6
     # Ceiling: one pinned cudaMemcpyAsync H2D of the same byte count.
     src_flat = pool.view(-1)[:nbytes]
     dst_flat = hot.view(-1)[:nbytes]
@@ -380,7 +399,7 @@ def bench_swapin(reps=10):
            "ceiling_memcpy_h2d_ms": c, "ceiling_gbs": nbytes / c / 1e6, "frac_of_ceiling": c / t,
            "backup_us": statistics.median(bt) * 1e3,
            "backup_ceiling_memcpy_d2h_us": statistics.median(bc) * 1e3,
-           "backup_bytes": R * ROW_BYTES}
+           "backup_bytes": R * ROW_BYTES, **parts}
     del hot, pool
     return res
 

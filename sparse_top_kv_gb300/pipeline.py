@@ -76,7 +76,7 @@ class HiSparseDecoder:
         self.side = torch.cuda.Stream(device=dev)
         self.ev_lists = torch.cuda.Event()
         self.ev_swapped = torch.cuda.Event()
-        self.ev_backup = torch.cuda.Event()
+        self.ev_row = torch.cuda.Event()
         # SMs left to the SwapIn while the resident-row attention runs (one
         # attention CTA per SM, one copy CTA per SM).
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -137,7 +137,15 @@ class HiSparseDecoder:
         # The model's KV write of the newest token (stand-in): reserved hot rows.
         with torch.cuda.stream(main):
             self.hot.index_copy_(0, self.reserved_rows, new_row)
+        self.ev_row.record(main)
         rec(0, main)
+        # Side stream, first: the BackUp of the new rows to their host rows,
+        # in the shadow of S1 and S2 (it needs only the row just written; the
+        # SwapIn of this step never reads those host rows, since S2 maps the
+        # newest token to its reserved row, never to a miss).
+        side.wait_event(self.ev_row)
+        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
+                  self.host_rows, status=self.status, stream=side)
         tok, slot, count, err = hs.normalize_indices(
             cand, self.row_req, seq_lens, self.block_table, self.page_size,
             window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
@@ -149,10 +157,7 @@ class HiSparseDecoder:
                                            stream=main)
         rec(2, main)
         self.ev_lists.record(main)
-        # Side stream: host-link traffic.  The SwapIn first (the step waits
-        # for it); the BackUp of the new rows after it, in the shadow of the
-        # attention over the swapped rows (no row this step reads comes from
-        # the host rows it writes).
+        # Side stream, then: the SwapIn of the misses (the step waits for it).
         side.wait_event(self.ev_lists)
         rec(3, side)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
@@ -161,9 +166,6 @@ class HiSparseDecoder:
                    status=self.status, stream=side)
         rec(4, side)
         self.ev_swapped.record(side)
-        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
-                  self.host_rows, status=self.status, stream=side)
-        self.ev_backup.record(side)
         # Main stream: HBM traffic over the resident rows meanwhile.
         qv = self.q_view(q)
         nkv = self.hot.shape[0]
@@ -172,14 +174,13 @@ class HiSparseDecoder:
                                  self.d_v, self.part_m, self.part_l, self.part_o, 0,
                                  status=self.status, stream=main)
         rec(5, main)
-        main.wait_event(self.ev_swapped)
+        main.wait_event(self.ev_swapped)  # also joins the side stream: its last work is the SwapIn
         # The swapped rows, merged with the resident-row states (eq. 7).
         hs.sparse_decode_finish(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                 miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),
                                 self.scale, self.d_v, self.part_m, self.part_l, self.part_o,
                                 self.parts_hit, sync=self.sync, out=self.out, lse=self.lse,
                                 status=self.status, stream=main)
-        main.wait_event(self.ev_backup)
         rec(6, main)
         return self.out, self.lse
 
