@@ -253,7 +253,7 @@ def run_full(args, rank, world, flush):
             dec.replay_packed(packed[s])
             torch.cuda.synchronize()
             e = lambda i, j: gev[i].elapsed_time(gev[j])  # noqa: E731
-            # S1, S2, side-stream start latency, SwapIn, resident rows,
+            # S1, S2, SwapIn start latency, SwapIn, resident rows,
             # swapped rows + merge (+ BackUp behind it), whole step.
             stage_ms += np.array([e(0, 1), e(1, 2), e(2, 3), e(3, 4), e(2, 5),
                                   min(e(4, 6), e(5, 6)), e(0, 6)])
@@ -719,9 +719,9 @@ def main():
         "stage_us_note": "timed steps replay one CUDA graph per step; stage_us from "
                          + full["stage_src"],
         "stage_us": {"s1_normalize": stage[0] * 1e3, "s2_lookup": stage[1] * 1e3,
-                     "side stream start": stage[2] * 1e3,
-                     "s3_swap_in (side stream)": stage[3] * 1e3,
-                     "s4_resident_rows (overlaps the swap)": stage[4] * 1e3,
+                     "swap start": stage[2] * 1e3,
+                     "s3_swap_in": stage[3] * 1e3,
+                     "s4_resident_rows (side stream, overlaps the swap)": stage[4] * 1e3,
                      "s4_swapped_rows_and_merge": stage[5] * 1e3, "step": stage[6] * 1e3},
         "hit_rate": full["hit_rate"],
         "roofline": dominant,

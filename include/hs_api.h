@@ -264,8 +264,10 @@ int hs_sparse_decode_partial(const void* q, const void* k_base, const void* v_ba
  * and lse (fp32 [rows, heads], natural log, or NULL).  Columns
  * [parts_used, parts_total) may be used as scratch: parts_total must be at
  * least parts_used + hs_sparse_decode_partial_splits(...).
- * sync: NULL, or int32 scratch of rows * heads words, zeroed by this call on
- * the stream before the launch.  For the MLA shape on tensor cores, with sync
+ * sync: NULL, or int32 counters of rows * heads words that are zero on entry
+ * (zero them once); every call that completes leaves them zero again (the
+ * last split of each (row, head group) resets its counter), so consecutive
+ * calls need no memset.  For the MLA shape on tensor cores, with sync
  * the new rows are split over several CTAs per (row, group of query heads);
  * each writes its partial column and the last to finish merges every column
  * in its epilogue (one launch).  Without sync (or when the split count plus

@@ -69,6 +69,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // G query heads of one KV head, rows of DQK (K) / DV (V) bf16 elements.
 template <int DQK, int DV, int G, bool SHARED_KV, int U>
 __global__ void __launch_bounds__(kThreads) attn_cc_kernel(const AttnArgs a) {
+    hs::pdl_trigger();
     constexpr int NQ = DQK / 64;
     constexpr int NV = DV / 64;
     extern __shared__ __align__(16) float red[];  // [kWarps][G][DV] + m,l [kWarps][G]
@@ -284,6 +285,7 @@ __global__ void merge_kernel(const float* __restrict__ pm, const float* __restri
                              const float* __restrict__ po, int32_t parts, int32_t d_v,
                              __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                              int32_t stride) {
+    hs::pdl_trigger();
     const int64_t n = blockIdx.x;
     const float* m = pm + n * stride;
     const float* l = pl + n * stride;
@@ -453,6 +455,7 @@ constexpr size_t gqa_smem_bytes() {
 
 template <int G, int W, int S>
 __global__ void __launch_bounds__(W * 32) attn_gqa_kernel(const AttnArgs a) {
+    hs::pdl_trigger();
     static_assert(G >= 1 && G <= 8, "a head group fills at most half of the MMA rows");
     constexpr int D = 128;
     extern __shared__ __align__(128) unsigned char gsm[];
@@ -663,7 +666,10 @@ __global__ void __launch_bounds__(W * 32) attn_gqa_kernel(const AttnArgs a) {
     __shared__ int last_split;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) last_split = atomicAdd(a.sync + unit, 1) == a.splits - 1;
+    if (threadIdx.x == 0) {
+        last_split = atomicAdd(a.sync + unit, 1) == a.splits - 1;
+        if (last_split) a.sync[unit] = 0;  // every split has arrived: reset for the next call
+    }
     __syncthreads();
     if (!last_split) return;
     __threadfence();
@@ -853,7 +859,11 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
     a.status = status;
     const int units = rows * kv_heads * p.chunks_per_kvh;
     a.sync = sync;
-    if (sync != nullptr &&
+    // Counters in the workspace are zeroed here; the caller's counters of the
+    // finishing pass are zero on entry, and every launch leaves them zero
+    // (the last split resets its counter), so no memset node separates that
+    // launch from its stream predecessor.
+    if (sync != nullptr && po == nullptr &&
         cudaMemsetAsync(sync, 0, size_t(units) * sizeof(int32_t),
                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return HS_ERR_CUDA;

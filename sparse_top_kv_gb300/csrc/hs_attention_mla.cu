@@ -155,16 +155,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
     const int row = blockIdx.x / groups;
     const int grp = blockIdx.x % groups;
     const int split = blockIdx.y;
-    const int n = a.count ? min(max(a.count[row], 0), a.cap) : a.cap;
-    const int ntiles = (n + kTok - 1) / kTok;
-    const int per = (ntiles + a.splits - 1) / a.splits;
-    const int t_begin = min(ntiles, split * per);
-    const int T = min(ntiles, t_begin + per) - t_begin;  // tiles of this CTA
     const int32_t* kv_rows = a.kv_rows + int64_t(row) * a.cap;
     const int head0 = grp * HG;
     const uint64_t tmo = a.timeout_ns;
     volatile int* abort_flag = &B.abort;
 
+    // Set-up that needs nothing from the stream predecessor (barriers, TMEM,
+    // the query) runs before pdl_wait.
+    hs::pdl_trigger();
     if (tid == 0) {
         for (int i = 0; i < NU; ++i) {
             hs::mbar_init(&B.full[i][0], kLoaderThreads);
@@ -200,6 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
         hs::tc::cp_async_wait_all();
         hs::fence_proxy_async_shared();
     }
+    hs::pdl_wait();
+    const int n = a.count ? min(max(a.count[row], 0), a.cap) : a.cap;
+    const int ntiles = (n + kTok - 1) / kTok;
+    const int per = (ntiles + a.splits - 1) / a.splits;
+    const int t_begin = min(ntiles, split * per);
+    const int T = min(ntiles, t_begin + per) - t_begin;  // tiles of this CTA
     hs::tc::fence_before_sync();
     __syncthreads();
     hs::tc::fence_after_sync();
@@ -641,6 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                         if (tid == 0) {
                             const int old = atomicAdd(a.sync + blockIdx.x, 1);
                             B.last = old == a.splits - 1 ? 1 : 0;
+                            // Every split has arrived: the counter is reset
+                            // for the next call.
+                            if (old == a.splits - 1) a.sync[blockIdx.x] = 0;
                         }
                         synced = all_sync();
                         last = synced && B.last != 0;
@@ -748,8 +755,7 @@ int launch_hg(const MlaArgs& a, dim3 grid, hs_stream_t stream) {
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(mla_tc_kernel<HG>),
                                                 smem, smem_set);
     if (rc != HS_OK) return rc;
-    mla_tc_kernel<HG><<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return hs_host::launch_status();
+    return hs_host::launch_pdl(mla_tc_kernel<HG>, grid, dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace

@@ -175,6 +175,20 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
     return res;
 }
 
+// ----------------------------------------------------------------------------
+// Programmatic dependent launch (PTX griddepcontrol).  Every kernel of the
+// library lets its dependents start launching at once (pdl_trigger), and
+// the kernels on the decode step's critical path are launched with
+// programmatic stream serialization, so each may start while its stream
+// predecessor still runs.  Rule kept by every such kernel: before pdl_wait
+// it writes no global memory and reads only inputs that no kernel of this
+// library writes (the query); pdl_wait returns once the predecessor grid has
+// completed and its writes are visible (at once when there is none).
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Default time limit of every bounded wait in this library (wall time).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
@@ -194,6 +208,28 @@ int ensure_dynamic_smem(const void* func, size_t bytes, int* cache /* [64] */);
 inline int launch_status() {
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+// Launch with programmatic stream serialization (the kernel follows the
+// pdl_trigger / pdl_wait rule above).
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, hs_stream_t stream,
+               Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) {
+        cudaGetLastError();
+        return HS_ERR_CUDA;
+    }
+    return HS_OK;
 }
 
 }  // namespace hs_host

@@ -107,8 +107,15 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     int16_t* H = E + hot_size;
     uint8_t* kind = reinterpret_cast<uint8_t*>(H + hot_size);  // kNone / kHit / kMiss
 
+    hs::pdl_trigger();
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
+    // Before the predecessor has completed: only the hash is cleared.
+    for (int h = tid * 4; h < HS; h += kThreads * 4) {
+        *reinterpret_cast<int4*>(keys + h) = make_int4(kEmpty, kEmpty, kEmpty, kEmpty);
+        *reinterpret_cast<int4*>(vals + h) = make_int4(INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX);
+    }
+    hs::pdl_wait();
     const int32_t* g_row = a.slot + int64_t(row) * cap;
     int32_t* out = a.hot_idx + int64_t(row) * cap;
     uint8_t* mm = a.miss_mask ? a.miss_mask + int64_t(row) * cap : nullptr;
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     const int64_t hot_base = int64_t(row) * a.region_stride;
 
     // Every global read of the kernel is issued here, in one batch: the
-    // row's state, its pending ids and its count; the hash is cleared.
+    // row's state, its pending ids and its count.
     const int n = a.count ? min(max(a.count[row], 0), cap) : cap;
     const int32_t newest = a.newest_slot ? a.newest_slot[row] : -1;
     for (int j = tid; j < hot_size; j += kThreads) {
@@ -145,10 +152,6 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         s_lru[j] = lru[j];
     }
     for (int i = tid; i < cap; i += kThreads) state[i] = g_row[i];
-    for (int h = tid * 4; h < HS; h += kThreads * 4) {
-        *reinterpret_cast<int4*>(keys + h) = make_int4(kEmpty, kEmpty, kEmpty, kEmpty);
-        *reinterpret_cast<int4*>(vals + h) = make_int4(INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX);
-    }
     if (tid == 0) s_dup = 0;
     __syncthreads();
 
@@ -299,6 +302,7 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
 }
 
 __global__ void reset_kernel(int32_t* dgi, int16_t* lru, int32_t hot_size) {
+    hs::pdl_trigger();
     const int64_t base = int64_t(blockIdx.x) * hot_size;
     for (int j = threadIdx.x; j < hot_size; j += blockDim.x) {
         dgi[base + j] = -1;
@@ -351,6 +355,5 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
                  dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
                  miss_src, miss_dst, miss_count, stats,    err,           log2n,
                  hit_idx,  miss_rows};
-    lookup_kernel<<<rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return hs_host::launch_status();
+    return hs_host::launch_pdl(lookup_kernel, dim3(rows), dim3(kThreads), smem, stream, a);
 }

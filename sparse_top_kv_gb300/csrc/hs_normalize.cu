@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
     __shared__ int scan_scratch[33];
     __shared__ int s_err[4];
 
+    hs::pdl_trigger();
+    hs::pdl_wait();
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
     const int32_t* cand = a.cand + int64_t(row) * a.n_cand;
@@ -264,6 +266,5 @@ extern "C" int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(normalize_kernel),
                                                 smem, smem_set);
     if (rc != HS_OK) return rc;
-    normalize_kernel<<<rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return hs_host::launch_status();
+    return hs_host::launch_pdl(normalize_kernel, dim3(rows), dim3(kThreads), smem, stream, a);
 }

@@ -97,10 +97,12 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WarpRing& R = rings[warp];
     unsigned char* ring = dsmem + size_t(warp) * kWS * kStageBytes;
+    hs::pdl_trigger();
     if (lane == 0) {
         for (int s = 0; s < kWS; ++s) hs::mbar_init(&R.full[s], 32);
         hs::fence_mbar_init();
     }
+    hs::pdl_wait();  // the lists and counts come from the predecessor
     // Groups per list -> prefix sums (warp 0).
     if (warp == 0) {
         int running = 0;
@@ -236,8 +238,7 @@ int launch_xfer(XferArgs a, int64_t max_items_rows, int max_ctas, hs_stream_t st
     // One CTA (192 KB of stages) per SM.
     const int64_t budget = max_ctas > 0 ? max_ctas : int64_t(hs_host::num_sms());
     const int64_t grid = hs::max64(1, hs::min64((groups + kWarps - 1) / kWarps, budget));
-    xfer_kernel<<<int(grid), kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return hs_host::launch_status();
+    return hs_host::launch_pdl(xfer_kernel, dim3(unsigned(grid)), dim3(kThreads), smem, stream, a);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -75,7 +75,7 @@ class HiSparseDecoder:
         self.part_o = torch.empty(R * heads, P, d_v, **f32)
         self.side = torch.cuda.Stream(device=dev)
         self.ev_lists = torch.cuda.Event()
-        self.ev_swapped = torch.cuda.Event()
+        self.ev_attn = torch.cuda.Event()
         self.ev_row = torch.cuda.Event()
         # SMs left to the SwapIn while the resident-row attention runs (one
         # attention CTA per SM, one copy CTA per SM).
@@ -123,13 +123,14 @@ class HiSparseDecoder:
         [R]; new_row [R, row_width] (the new token's KV row); q bf16 [R, H, d_qk].
         Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated.
 
-        The SwapIn and BackUp run on a side stream, concurrently with the
-        attention over the rows that were already resident (hit_idx); the
-        attention over the swapped rows (miss_rows) follows the SwapIn, and the
-        two sets of partial states are merged with eq. (7).
+        The SwapIn runs concurrently with the attention over the rows that
+        were already resident (hit_idx, side stream); the attention over the
+        swapped rows (miss_rows) follows the SwapIn, and the two sets of
+        partial states are merged with eq. (7).  The BackUp runs on the side
+        stream during S1 and S2.
         `events`, if given, is a list of 7 CUDA events recorded before S1, after
-        S1, after S2, before and after SwapIn (side stream), after the
-        resident-row attention and at the end of the step."""
+        S1, after S2, before and after SwapIn, after the resident-row attention
+        (side stream) and at the end of the step."""
         R = self.num_reqs
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side
@@ -157,24 +158,28 @@ class HiSparseDecoder:
                                            stream=main)
         rec(2, main)
         self.ev_lists.record(main)
-        # Side stream, then: the SwapIn of the misses (the step waits for it).
-        side.wait_event(self.ev_lists)
-        rec(3, side)
+        # Main stream: the SwapIn of the misses right behind S2, then the
+        # swapped rows' attention right behind the SwapIn; these three are
+        # the step's critical path and each may start (set-up only) while its
+        # predecessor runs (programmatic dependent launch).
+        rec(3, main)
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
                    region_stride=self.region_stride, max_ctas=self.swap_ctas,
-                   status=self.status, stream=side)
-        rec(4, side)
-        self.ev_swapped.record(side)
-        # Main stream: HBM traffic over the resident rows meanwhile.
+                   status=self.status, stream=main)
+        rec(4, main)
+        # Side stream: HBM traffic over the resident rows meanwhile, on the
+        # SMs the SwapIn leaves free.
         qv = self.q_view(q)
         nkv = self.hot.shape[0]
+        side.wait_event(self.ev_lists)
         hs.sparse_decode_partial(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                  hit_idx.view(R, 1, self.cap), count.view(R, 1), self.scale,
                                  self.d_v, self.part_m, self.part_l, self.part_o, 0,
-                                 status=self.status, stream=main)
-        rec(5, main)
-        main.wait_event(self.ev_swapped)  # also joins the side stream: its last work is the SwapIn
+                                 status=self.status, stream=side)
+        rec(5, side)
+        self.ev_attn.record(side)
+        main.wait_event(self.ev_attn)  # also joins the side stream: its last work
         # The swapped rows, merged with the resident-row states (eq. 7).
         hs.sparse_decode_finish(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                 miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),

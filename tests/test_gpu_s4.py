@@ -177,11 +177,15 @@ def test_partial_passes_merge_to_the_full_set(heads, d):
     out2, lse2 = hs.sparse_decode_finish(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb),
                                          1 / math.sqrt(d), d_v, pm, pl, po, pa, status=status)
     # The split last pass: several CTAs per row, the last to arrive merges.
-    sync = torch.full((rows * H,), 7, dtype=torch.int32, device="cuda")  # zeroed by the call
-    out3, lse3 = hs.sparse_decode_finish(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb),
-                                         1 / math.sqrt(d), d_v, pm, pl, po, pa, sync=sync,
-                                         status=status)
+    # The counters are zero on entry and every call leaves them zero: two
+    # calls in a row, no reset in between.
+    sync = torch.zeros((rows * H,), dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        out3, lse3 = hs.sparse_decode_finish(q, k, v, rs, hsd, nkv, cuda(b), cuda(cb),
+                                             1 / math.sqrt(d), d_v, pm, pl, po, pa, sync=sync,
+                                             status=status)
     torch.cuda.synchronize()
+    assert int(sync.abs().sum().item()) == 0
     assert status.item() == 0
     sample = [0, 7, rows - 1]
     kb = bits(k).reshape(-1)
