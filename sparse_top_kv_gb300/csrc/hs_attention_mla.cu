@@ -204,6 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
     const int per = (ntiles + a.splits - 1) / a.splits;
     const int t_begin = min(ntiles, split * per);
     const int T = min(ntiles, t_begin + per) - t_begin;  // tiles of this CTA
+    // A CTA with one tile keeps the four K-pair units of QK(0) (blocks 0-7 =
+    // the V columns) for PV(0) instead of gathering V again, when the ring
+    // holds all five QK units at once (16 and 32 heads per CTA); with more
+    // tiles the ring is needed for the next QK, so V is re-gathered.
+    const bool reuse_v = T == 1 && NU >= kQkUnits;
     hs::tc::fence_before_sync();
     __syncthreads();
     hs::tc::fence_after_sync();
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             }
             fetch(t + 3, id_far);
             if (t + 1 < T) ok = load_qk(t + 1, id_cur);
-            if (ok) ok = load_pv(t, id_prev);
+            if (ok && !reuse_v) ok = load_pv(t, id_prev);
         }
         if (!ok) {
             hs::set_status(a.status, HS_ERR_TIMEOUT);
@@ -315,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                         hs::tc::mma_bf16(tmem + C::kS + sb * HG, ad, bd, idesc_qk,
                                          (b | kk) ? 1u : 0u);
                     }
-                    if ((b & 1) || b == kNB - 1) hs::tc::mma_commit(&B.empty[k % NU]);
+                    if (((b & 1) && !reuse_v) || b == kNB - 1)
+                        hs::tc::mma_commit(&B.empty[k % NU]);
                 }
                 hs::tc::mma_commit(&B.s_full[sb]);
                 return true;
@@ -323,7 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             auto issue_pv = [&](int t) -> bool {
                 if (!hs::mbar_wait_bounded(&B.p_full, t & 1, tmo, abort_flag)) return false;
                 hs::tc::fence_after_sync();
-                const int k0 = unit_seq(t, 1, 0, T);
+                // V from the QK units themselves (one tile: their full
+                // barriers' phases have completed) or from the PV units.
+                const int k0 = reuse_v ? unit_seq(t, 0, 0, T) : unit_seq(t, 1, 0, T);
 #pragma unroll 1
                 for (int cs = 0; cs < kPvUnits; ++cs) {
                     const int k = k0 + cs;
