@@ -330,12 +330,14 @@ def bench_swapin(reps=10):
     mcount = torch.full((R,), M, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     pdev = hs.host_device_pointer(pool)
+    ticket = torch.zeros(2, dtype=torch.int32, device="cuda")
     nbytes = R * M * ROW_BYTES
     times = []
     for i in range(reps + 3):
         a, b = ev(), ev()
         a.record()
-        hs.swap_in(pdev, pool.shape[0], hot, ROW_BYTES, msrc, mdst, mcount, status=status)
+        hs.swap_in(pdev, pool.shape[0], hot, ROW_BYTES, msrc, mdst, mcount, ticket=ticket,
+                   status=status)
         b.record()
         b.synchronize()
         if i >= 3:
@@ -352,7 +354,7 @@ def bench_swapin(reps=10):
                 a, b = ev(), ev()
                 a.record()
                 hs.swap_in(pdev, pool.shape[0], hot, ROW_BYTES, msrc, mdst, cnt,
-                           max_ctas=ctas, status=status)
+                           max_ctas=ctas, ticket=ticket, status=status)
                 b.record()
                 b.synchronize()
                 if i >= 3:

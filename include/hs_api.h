@@ -164,6 +164,11 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
  *             ([HC] Motivation: the copy's SM footprint is the cost to the
  *             concurrent forward pass); a few dozen CTAs already keep enough
  *             bytes in flight to fill the host link.
+ * ticket      NULL (groups of rows dealt round-robin to the warps), or int32
+ *             [2] device counters, zero on entry (zero them once), that the
+ *             call leaves zero: warps then claim groups one at a time, so a
+ *             warp that runs ahead takes more and the copy ends together.
+ *             Calls that may run at the same time need their own counters.
  * status      int32 device word or NULL: HS_ERR_TIMEOUT / HS_ERR_BAD_INDEX
  *             is stored there (first error wins) if the device hits one.
  * Destinations must be distinct within one call.
@@ -171,7 +176,7 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
 int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, int64_t row_bytes,
                const int32_t* miss_src, const int64_t* miss_dst, const int32_t* miss_count,
                int32_t rows, int32_t cap, int32_t* dgi, int32_t hot_size, int64_t region_stride,
-               int32_t max_ctas, int32_t* status, hs_stream_t stream);
+               int32_t max_ctas, int32_t* ticket, int32_t* status, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * hs_backup -- [HS] overview "BackUp": after each step copy the newly

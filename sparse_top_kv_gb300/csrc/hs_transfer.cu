@@ -61,6 +61,7 @@ struct XferArgs {
     int64_t region_stride;
     int32_t* status;
     uint64_t timeout_ns;
+    int32_t* ticket;        // [2] claim and exit counters (zero on entry, left zero), or nullptr
 };
 
 struct WarpRing {
@@ -121,15 +122,26 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
     const int nv = int(rb / 16);
     const int gw = blockIdx.x * kWarps + warp;   // global warp id
     const int nw = gridDim.x * kWarps;
-    const int mine = gw < total ? (total - gw + nw - 1) / nw : 0;  // groups of this warp
+    // Groups of this warp: round-robin over the grid, or, with a ticket
+    // counter, claimed one at a time (a warp that runs ahead takes more, so
+    // the copy ends together); `mine` is then fixed at the first claim past
+    // the last group.
+    const bool claim = a.ticket != nullptr;
+    int mine = claim ? (1 << 30) : (gw < total ? (total - gw + nw - 1) / nw : 0);
     bool ok = true;
     bool bad = false;
     for (int j = 0; j < mine + kWS - 1 && ok; ++j) {
         // (a) Issue group j into stage j % kWS.
+        int gidx = gw + j * nw;
+        if (claim && j < mine) {
+            int t = 0;
+            if (lane == 0) t = atomicAdd(a.ticket, 1);
+            gidx = __shfl_sync(0xffffffffu, t, 0);
+            if (gidx >= total) mine = j;
+        }
         if (j < mine) {
             const int st = j % kWS;
             unsigned char* stage = ring + size_t(st) * kStageBytes;
-            const int gidx = gw + j * nw;
             int lo = 0, hi = a.nlists;
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
@@ -215,6 +227,15 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
     }
     if (!ok) hs::set_status(a.status, HS_ERR_TIMEOUT);
     if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+    if (claim && lane == 0) {
+        // Every warp has made its last claim before it counts itself out; the
+        // last one out resets both counters for the next launch.
+        __threadfence();
+        if (atomicAdd(a.ticket + 1, 1) == nw - 1) {
+            a.ticket[0] = 0;
+            a.ticket[1] = 0;
+        }
+    }
     // Leave no copy into shared memory in flight (bounded: the waits above
     // only give up after the wall-time limit).
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -249,7 +270,7 @@ extern "C" int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, i
                           const int32_t* miss_src, const int64_t* miss_dst,
                           const int32_t* miss_count, int32_t rows, int32_t cap, int32_t* dgi,
                           int32_t hot_size, int64_t region_stride, int32_t max_ctas,
-                          int32_t* status, hs_stream_t stream) {
+                          int32_t* ticket, int32_t* status, hs_stream_t stream) {
     if (rows < 0 || cap < 0 || host_rows < 0 || row_bytes <= 0 || max_ctas < 0)
         return HS_ERR_INVALID_ARG;
     if (row_bytes % 16 != 0) return HS_ERR_MISALIGNED;
@@ -277,6 +298,7 @@ extern "C" int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, i
     a.region_stride = region_stride;
     a.status = status;
     a.timeout_ns = hs::kWaitTimeoutNs;
+    a.ticket = ticket;
     return launch_xfer(a, int64_t(rows) * cap, max_ctas, stream);
 }
 

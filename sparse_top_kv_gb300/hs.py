@@ -38,7 +38,7 @@ _SIGS = {
     "hs_hot_state_reset": ([_P, _P, _I32, _I32, _P], ctypes.c_int),
     "hs_hot_lookup_assign": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
                               _P, _P, _P, _P, _P, _P], ctypes.c_int),
-    "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _I32, _P, _P],
+    "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _I32, _P, _P, _P],
                    ctypes.c_int),
     "hs_backup": ([_P, _P, _P, _P, _I32, _I64, _I64, _P, _P], ctypes.c_int),
     "hs_sparse_decode_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32], _I64),
@@ -187,17 +187,23 @@ def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, 
 
 
 def swap_in(host_pool_dev, host_rows, hot, row_bytes, miss_src, miss_dst, miss_count, *,
-            dgi=None, hot_size=0, region_stride=0, max_ctas=0, status=None, stream=None):
-    """S3 SwapIn.  host_pool_dev: device-visible address (int) of the pinned pool."""
+            dgi=None, hot_size=0, region_stride=0, max_ctas=0, ticket=None, status=None,
+            stream=None):
+    """S3 SwapIn.  host_pool_dev: device-visible address (int) of the pinned pool.
+    ticket: None, or int32 [2] device counters, zero on entry and left zero
+    (groups claimed dynamically by the warps)."""
     _check(miss_src, torch.int32, "miss_src")
     _check(miss_dst, torch.int64, "miss_dst")
     _check(miss_count, torch.int32, "miss_count")
     _check(dgi, torch.int32, "dgi")
+    _check(ticket, torch.int32, "ticket")
     _check(status, torch.int32, "status")
+    if ticket is not None and ticket.numel() < 2:
+        raise ValueError("ticket needs 2 int32 words")
     rows, cap = miss_src.shape
     _call("hs_swap_in", ctypes.c_void_p(host_pool_dev), host_rows, _ptr(hot), row_bytes,
           _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), rows, cap, _ptr(dgi), hot_size,
-          region_stride, max_ctas, _ptr(status), _stream(stream))
+          region_stride, max_ctas, _ptr(ticket), _ptr(status), _stream(stream))
 
 
 def backup(src, src_rows, host_pool_dev, dst_slots, row_bytes, host_rows, *, status=None,

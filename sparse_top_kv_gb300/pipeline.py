@@ -70,6 +70,7 @@ class HiSparseDecoder:
         f32 = dict(dtype=torch.float32, device=dev)
         # Arrival counters of the finishing pass's last-CTA merge.
         self.sync = torch.zeros(R * heads, dtype=torch.int32, device=dev)
+        self.ticket = torch.zeros(2, dtype=torch.int32, device=dev)  # SwapIn group claims
         self.part_m = torch.empty(R * heads, P, **f32)
         self.part_l = torch.empty(R * heads, P, **f32)
         self.part_o = torch.empty(R * heads, P, d_v, **f32)
@@ -166,7 +167,7 @@ class HiSparseDecoder:
         hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
                    miss_count, dgi=self.dgi, hot_size=self.hot_size,
                    region_stride=self.region_stride, max_ctas=self.swap_ctas,
-                   status=self.status, stream=main)
+                   ticket=self.ticket, status=self.status, stream=main)
         rec(4, main)
         # Side stream: HBM traffic over the resident rows meanwhile, on the
         # SMs the SwapIn leaves free.

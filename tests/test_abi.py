@@ -50,8 +50,8 @@ def test_host_side_argument_checks():
                                   P) == 1
     assert L.hs_hot_state_reset(P, P, 1, 40000, P) == 1
     # Rows not a multiple of 16 bytes.
-    assert L.hs_swap_in(P, 10, P, 100, P, P, P, 1, 1, P, 0, 0, 0, P, P) == 2
-    assert L.hs_swap_in(P, 10, P, 96, P, P, P, 1, 1, P, 0, 0, -1, P, P) == 1
+    assert L.hs_swap_in(P, 10, P, 100, P, P, P, 1, 1, P, 0, 0, 0, P, P, P) == 2
+    assert L.hs_swap_in(P, 10, P, 96, P, P, P, 1, 1, P, 0, 0, -1, P, P, P) == 1
     assert L.hs_backup(P, P, P, P, 1, 24, 10, P, P) == 2
     # Unsupported attention shape, null pointers.
     buf = ctypes.create_string_buffer(4096)

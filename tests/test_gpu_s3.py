@@ -18,7 +18,8 @@ def pinned_random(rows, rb, seed):
     return t.pin_memory()
 
 
-def swap_both(pool, hot_init, rb, msrc, mdst, mcount, dgi=None, hot_size=0, region=0):
+def swap_both(pool, hot_init, rb, msrc, mdst, mcount, dgi=None, hot_size=0, region=0,
+              ticket=None, max_ctas=0):
     hot_ref = hot_init.copy()
     dgi_ref = None if dgi is None else dgi.copy()
     oracle.swap_in(pool.numpy().reshape(-1), hot_ref.reshape(-1), rb, msrc, mdst, mcount,
@@ -27,16 +28,22 @@ def swap_both(pool, hot_init, rb, msrc, mdst, mcount, dgi=None, hot_size=0, regi
     gdgi = None if dgi is None else cuda(dgi)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     hs.swap_in(hs.host_device_pointer(pool), pool.shape[0], hot, rb, cuda(msrc), cuda(mdst),
-               cuda(mcount), dgi=gdgi, hot_size=hot_size, region_stride=region, status=status)
+               cuda(mcount), dgi=gdgi, hot_size=hot_size, region_stride=region,
+               max_ctas=max_ctas, ticket=ticket, status=status)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(u8(hot), hot_ref)
+    if ticket is not None:
+        assert ticket.tolist()[:2] == [0, 0]  # left zero for the next call
     if dgi is not None:
         np.testing.assert_array_equal(np_i32(gdgi), dgi_ref)
     return int(status.item())
 
 
-@pytest.mark.parametrize("rb", [16, 656, 1152, 4096])
-def test_runs_scattered_and_bad_sources(rb):
+@pytest.mark.parametrize("rb,claim", [(16, False), (656, False), (1152, False), (4096, False),
+                                      (1152, True), (16, True)])
+def test_runs_scattered_and_bad_sources(rb, claim):
+    """claim: groups claimed through ticket counters, on a budget of 3 SMs
+    (one counter pair serves both calls: each call leaves it zero)."""
     rng = np.random.default_rng(rb)
     pool_rows, rows, hot_size = 5000, 6, 300
     region = hot_size + 1
@@ -65,9 +72,11 @@ def test_runs_scattered_and_bad_sources(rb):
         mdst[r, :n] = r * region + dst
         counts[r] = n
     dgi = rng.integers(0, 10**6, size=(rows, hot_size)).astype(np.int32)
-    status = swap_both(pool, hot_init, rb, msrc, mdst, counts, dgi=dgi, hot_size=hot_size,
-                       region=region)
-    assert status == 0
+    ticket = torch.zeros(2, dtype=torch.int32, device="cuda") if claim else None
+    for _ in range(2 if claim else 1):
+        status = swap_both(pool, hot_init, rb, msrc, mdst, counts, dgi=dgi, hot_size=hot_size,
+                           region=region, ticket=ticket, max_ctas=3 if claim else 0)
+        assert status == 0
 
 
 def test_backup_and_bad_destination():
@@ -99,6 +108,9 @@ def test_swapin_config_full_size():
     counts = np.full(R, M, np.int32)
     hot_init = np.zeros((R * region, rb), np.uint8)
     assert swap_both(pool, hot_init, rb, msrc, mdst, counts) == 0
+    # The step's launch: 24 SMs, groups claimed through ticket counters.
+    ticket = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert swap_both(pool, hot_init, rb, msrc, mdst, counts, ticket=ticket, max_ctas=24) == 0
     # BackUp: the reserved row of each request -> random host slots.
     src = cuda(np.random.default_rng(5).integers(0, 256, size=(R * region, rb), dtype=np.uint8))
     src_rows = np.arange(R, dtype=np.int64) * region + M
