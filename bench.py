@@ -34,7 +34,7 @@ ROW_BYTES = 1152
 # DRAM bytes (read + write) per launch from the ncu capture summarised in
 # profiles/step_kernels_full_hisparse.md (set to None when a kernel changes
 # after the capture).
-NCU_TRAFFIC = {"attention": 131856640 + 19920384, "swap_in": 266752 + 9644544}
+NCU_TRAFFIC = {"attention": 131952128 + 19910912, "swap_in": 273408 + 9880832}
 
 
 def load_peaks():
