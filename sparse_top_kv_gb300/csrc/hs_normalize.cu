@@ -27,6 +27,7 @@ constexpr int kWindowWords = kThreads * kWordsPerThread;     // 4096 words = 16 
 constexpr int64_t kWindowBits = int64_t(kWindowWords) * 32;  // 131072 positions
 constexpr int kMaxStagedBlocks = 16384;  // block-table rows up to this are copied to smem
 constexpr int kUnroll = 4;               // candidates loaded per thread before use
+constexpr int kMaxOutStageBytes = 160 * 1024;  // dynamic shared memory for table + outputs
 
 struct NormArgs {
     const int32_t* cand;
@@ -44,6 +45,7 @@ struct NormArgs {
     int32_t* err_counts;
     int32_t stage_table;  // 1: the request's block-table row is staged in shared memory
     int32_t page_shift;   // log2(page_size) when it is a power of two, else -1
+    int32_t stage_out;    // 1: the outputs are assembled in shared memory, then written once
 };
 
 // Logical block and in-page offset of position t (0 <= t < 2^31): a shift and
@@ -74,7 +76,9 @@ __device__ __forceinline__ int classify_in_range(int64_t t, const int32_t* table
 }
 
 __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
-    extern __shared__ int32_t s_table[];  // [max_blocks] when a.stage_table
+    // Dynamic: [max_blocks] table when a.stage_table, then [cap] tokens and
+    // [cap] slots when a.stage_out.
+    extern __shared__ int32_t s_dyn[];
     __shared__ uint32_t bm[kWindowWords];
     __shared__ int wpos[kWindowWords];  // output offset of each bitmap word
     __shared__ int scan_scratch[33];
@@ -85,8 +89,24 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
     const int32_t* cand = a.cand + int64_t(row) * a.n_cand;
-    int32_t* otok = a.out_tok + int64_t(row) * a.cap;
-    int32_t* oslot = a.out_slot + int64_t(row) * a.cap;
+    int32_t* const g_tok = a.out_tok + int64_t(row) * a.cap;
+    int32_t* const g_slot = a.out_slot + int64_t(row) * a.cap;
+    int32_t* const s_table = s_dyn;
+    int32_t* const s_tok = s_dyn + (a.stage_table ? a.max_blocks : 0);
+    int32_t* const s_slot = s_tok + a.cap;
+    // Emission targets: shared memory (written out coalesced at the end) or
+    // the global rows directly.
+    int32_t* const otok = a.stage_out ? s_tok : g_tok;
+    int32_t* const oslot = a.stage_out ? s_slot : g_slot;
+    // The first kUnroll candidates of this thread, loaded before anything
+    // else (their latency overlaps the request lookups below); later chunks,
+    // if any, are loaded where they are used.
+    int32_t tv0[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int i = tid + u * kThreads;
+        tv0[u] = i < a.n_cand ? __ldg(cand + i) : -1;
+    }
     if (tid < 4) s_err[tid] = 0;
     __syncthreads();
 
@@ -117,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
                     const int i = i0 + u * kThreads;
-                    tv[u] = i < a.n_cand ? __ldg(cand + i) : -1;
+                    tv[u] = i0 == tid ? tv0[u] : (i < a.n_cand ? __ldg(cand + i) : -1);
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
@@ -161,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
                     const int i = i0 + u * kThreads;
-                    tv[u] = i < a.n_cand ? __ldg(cand + i) : -1;
+                    tv[u] = i0 == tid ? tv0[u] : (i < a.n_cand ? __ldg(cand + i) : -1);
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
@@ -222,9 +242,17 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
             __syncthreads();
         }
     }
-    for (int j = out_n + tid; j < a.cap; j += kThreads) {
-        otok[j] = -1;
-        oslot[j] = -1;
+    if (a.stage_out) {
+        __syncthreads();
+        for (int j = tid; j < a.cap; j += kThreads) {
+            g_tok[j] = j < out_n ? s_tok[j] : -1;
+            g_slot[j] = j < out_n ? s_slot[j] : -1;
+        }
+    } else {
+        for (int j = out_n + tid; j < a.cap; j += kThreads) {
+            g_tok[j] = -1;
+            g_slot[j] = -1;
+        }
     }
     __syncthreads();
     if (tid == 0) a.out_count[row] = out_n;
@@ -255,13 +283,18 @@ extern "C" int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n
     NormArgs a{cand,      rows,      n_cand,     window,    num_sinks, row_req,
                seq_lens,  block_table, bt_stride, max_blocks, page_owner, num_reqs,
                num_pages, page_size, cap,        out_tok,   out_slot,  out_count,
-               err_counts, max_blocks <= kMaxStagedBlocks ? 1 : 0, -1};
+               err_counts, max_blocks <= kMaxStagedBlocks ? 1 : 0, -1, 0};
     if ((page_size & (page_size - 1)) == 0) {
         int sh = 0;
         while ((1 << sh) < page_size) ++sh;
         a.page_shift = sh;
     }
-    const size_t smem = a.stage_table ? size_t(max_blocks) * sizeof(int32_t) : 0;
+    size_t smem = a.stage_table ? size_t(max_blocks) * sizeof(int32_t) : 0;
+    // Outputs assembled in shared memory when they fit beside the table.
+    if (smem + size_t(cap) * 2 * sizeof(int32_t) <= size_t(kMaxOutStageBytes)) {
+        a.stage_out = 1;
+        smem += size_t(cap) * 2 * sizeof(int32_t);
+    }
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(normalize_kernel),
                                                 smem, smem_set);

@@ -77,7 +77,6 @@ class HiSparseDecoder:
         self.side = torch.cuda.Stream(device=dev)
         self.ev_lists = torch.cuda.Event()
         self.ev_attn = torch.cuda.Event()
-        self.ev_row = torch.cuda.Event()
         # SMs left to the SwapIn while the resident-row attention runs (one
         # attention CTA per SM, one copy CTA per SM).
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -127,8 +126,8 @@ class HiSparseDecoder:
         The SwapIn runs concurrently with the attention over the rows that
         were already resident (hit_idx, side stream); the attention over the
         swapped rows (miss_rows) follows the SwapIn, and the two sets of
-        partial states are merged with eq. (7).  The BackUp runs on the side
-        stream during S1 and S2.
+        partial states are merged with eq. (7).  The new rows' write and
+        their BackUp run on the side stream ahead of that attention.
         `events`, if given, is a list of 7 CUDA events recorded before S1, after
         S1, after S2, before and after SwapIn, after the resident-row attention
         (side stream) and at the end of the step."""
@@ -136,18 +135,7 @@ class HiSparseDecoder:
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side
         rec = (lambda i, st: events[i].record(st)) if events is not None else (lambda i, st: None)
-        # The model's KV write of the newest token (stand-in): reserved hot rows.
-        with torch.cuda.stream(main):
-            self.hot.index_copy_(0, self.reserved_rows, new_row)
-        self.ev_row.record(main)
         rec(0, main)
-        # Side stream, first: the BackUp of the new rows to their host rows,
-        # in the shadow of S1 and S2 (it needs only the row just written; the
-        # SwapIn of this step never reads those host rows, since S2 maps the
-        # newest token to its reserved row, never to a miss).
-        side.wait_event(self.ev_row)
-        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
-                  self.host_rows, status=self.status, stream=side)
         tok, slot, count, err = hs.normalize_indices(
             cand, self.row_req, seq_lens, self.block_table, self.page_size,
             window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
@@ -169,11 +157,23 @@ class HiSparseDecoder:
                    region_stride=self.region_stride, max_ctas=self.swap_ctas,
                    ticket=self.ticket, status=self.status, stream=main)
         rec(4, main)
-        # Side stream: HBM traffic over the resident rows meanwhile, on the
-        # SMs the SwapIn leaves free.
+        # Side stream, once S2 has listed the misses (kernels beside S1 and
+        # S2 slowed them by ~5 us in the captured step, measured): the
+        # model's KV write of the newest token (stand-in: the reserved hot
+        # rows; only the attention passes read them, and both follow this
+        # stream), the BackUp of those rows to their host rows (this step's
+        # SwapIn never reads them: S2 maps the newest token to its reserved
+        # row, never to a miss), then the HBM traffic over the resident rows,
+        # on the SMs the SwapIn leaves free.
         qv = self.q_view(q)
         nkv = self.hot.shape[0]
         side.wait_event(self.ev_lists)
+        with torch.cuda.stream(side):
+            self.hot.index_copy_(0, self.reserved_rows, new_row)
+        if not torch.cuda.is_current_stream_capturing():
+            new_row.record_stream(side)  # the caller's tensor is read on the side stream
+        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
+                  self.host_rows, status=self.status, stream=side)
         hs.sparse_decode_partial(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                  hit_idx.view(R, 1, self.cap), count.view(R, 1), self.scale,
                                  self.d_v, self.part_m, self.part_l, self.part_o, 0,
