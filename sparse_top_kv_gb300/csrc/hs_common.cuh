@@ -153,26 +153,21 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
     return v;
 }
 
-// Block-wide exclusive scan of v over threadIdx.x order.  `scratch` holds
-// >= blockDim.x/32 + 1 ints of shared memory.  Returns the exclusive prefix;
-// *total receives the block sum.  Must be called by every thread.
+// Block-wide exclusive scan of v over threadIdx.x order with one barrier:
+// each warp publishes its total, then every warp scans the (at most 32) warp
+// totals itself.  `scratch` holds >= 32 ints of shared memory; *total
+// receives the block sum.  Must be called by every thread.  `scratch` is
+// read after the barrier, so a second call needs a barrier before it.
 __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = (blockDim.x + 31) >> 5;
     const int incl = warp_incl_scan(v);
     if (lane == 31) scratch[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        int w = lane < nwarps ? scratch[lane] : 0;
-        const int wi = warp_incl_scan(w);
-        if (lane < nwarps) scratch[lane] = wi - w;
-        if (lane == nwarps - 1) scratch[32] = wi;
-    }
-    __syncthreads();
-    const int res = scratch[warp] + incl - v;
-    *total = scratch[32];
-    __syncthreads();
-    return res;
+    const int w = lane < nwarps ? scratch[lane] : 0;
+    const int wi = warp_incl_scan(w);
+    *total = __shfl_sync(0xffffffffu, wi, nwarps - 1);
+    return __shfl_sync(0xffffffffu, wi - w, warp) + incl - v;
 }
 
 // ----------------------------------------------------------------------------

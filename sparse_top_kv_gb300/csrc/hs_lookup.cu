@@ -173,7 +173,10 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         }
     }
     __syncthreads();
-    // Repeats of an earlier pending id resolve to -1.
+    // Repeats of an earlier pending id resolve to -1.  This runs in the
+    // same phase as the LRU walk below: the walk writes only first
+    // occurrences (vals[h]) and this only later ones, and a first occurrence
+    // reads as pending or done here, never as a repeat.
     {
         int dups = 0;
         for (int i = tid; i < cap; i += kThreads) {
@@ -189,7 +192,6 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         }
         if (dups) atomicAdd(&s_dup, dups);
     }
-    __syncthreads();
 
     // Phase 2: LRU walk, least -> most recently used.  Thread t owns the
     // contiguous positions [t*K2, t*K2 + K2); one block scan orders hits and
@@ -215,8 +217,26 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         hitmask |= 1u << k;
         ++nh;
     }
-    int hits_total;
-    const int hexcl = hs::block_excl_scan(nh, scan_scratch, &hits_total);
+    __syncthreads();  // every hit and repeat is marked
+
+    // Phase 3 ranks the misses in row order: thread t owns the contiguous
+    // entries [t*K3, t*K3 + K3).  One block scan serves both orders: the hit
+    // count of the thread's LRU positions in the low 16 bits, its miss count
+    // in the high 16 (each total is at most hot_size <= 32767).
+    const int K3 = (cap + kThreads - 1) / kThreads;
+    const int i0 = tid * K3;
+    int nm = 0;
+    for (int k = 0; k < K3; ++k) {
+        const int i = i0 + k;
+        if (i >= cap) break;
+        nm += state[i] != kDone;
+    }
+    int packed_total;
+    const int packed = hs::block_excl_scan(nh | (nm << 16), scan_scratch, &packed_total);
+    const int hexcl = packed & 0xffff;
+    const int hits_total = packed_total & 0xffff;
+    const int miss_total = packed_total >> 16;
+    int m = packed >> 16;
     {
         int hp = hexcl, ep = min(p0, hot_size) - hexcl;
         for (int k = 0; k < K2; ++k) {
@@ -226,21 +246,10 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
             if ((hitmask >> k) & 1u) H[hp++] = sl; else E[ep++] = sl;
         }
     }
-    __syncthreads();
+    __syncthreads();  // E and H are complete
     const int nE = hot_size - hits_total;
 
-    // Phase 3: misses in row order take E[0], E[1], ...  Thread t owns the
-    // contiguous entries [t*K3, t*K3 + K3).
-    const int K3 = (cap + kThreads - 1) / kThreads;
-    const int i0 = tid * K3;
-    int nm = 0;
-    for (int k = 0; k < K3; ++k) {
-        const int i = i0 + k;
-        if (i >= cap) break;
-        nm += state[i] != kDone;
-    }
-    int miss_total;
-    int m = hs::block_excl_scan(nm, scan_scratch, &miss_total);
+    // Misses in row order take E[0], E[1], ...
     for (int k = 0; k < K3; ++k) {
         const int i = i0 + k;
         if (i >= cap) break;
