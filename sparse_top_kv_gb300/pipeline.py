@@ -218,7 +218,7 @@ class HiSparseDecoder:
             out[off:off + nbytes].view(dt).view(shape).copy_(t.reshape(shape))
         return out
 
-    def capture(self, events=None):
+    def capture(self, events=None, slot=None):
         """Capture one decode step over static input buffers (`self.graph_in`,
         views of the packed buffer `self.graph_in_packed`) as a CUDA graph,
         both streams included.  `replay(...)` / `replay_packed(...)` then copy
@@ -226,21 +226,38 @@ class HiSparseDecoder:
         launch.  Run at least one eager step first (it performs the one-time
         library set-up that capture must not do).  `events`, if given, are
         timing events recorded inside the graph (see `step`).  Returns the
-        graph (also kept as self.graph, the one replay uses)."""
+        graph (also kept as self.graph, the one replay uses).
+
+        `slot`, if given, is a device buffer in the packed layout
+        (`pack_inputs`) that the graph reads its inputs from in place: an
+        engine that keeps each step's inputs in graph-stable slots (the model
+        writes the next step's inputs into a slot) replays one such graph per
+        slot with no staging copy.  That graph is returned and not kept."""
         dev = self.device
-        if getattr(self, "graph_in_packed", None) is None:
-            layout, total = self._input_layout()
-            self.graph_in_packed = torch.empty(total, dtype=torch.uint8, device=dev)
-            self.graph_in = {name: self.graph_in_packed[off:off + nb].view(dt).view(shape)
-                             for name, off, shape, dt, nb in layout}
-        gi = self.graph_in
+        if slot is None:
+            if getattr(self, "graph_in_packed", None) is None:
+                layout, total = self._input_layout()
+                self.graph_in_packed = torch.empty(total, dtype=torch.uint8, device=dev)
+                self.graph_in = self.input_views(self.graph_in_packed)
+            gi = self.graph_in
+        else:
+            gi = self.input_views(slot)
         g = torch.cuda.CUDAGraph()
         self.side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.graph(g):
             self.step(gi["cand"], gi["seq"], gi["newest"], gi["new_row"], gi["q"],
                       events=events)
-        self.graph = g
+        if slot is None:
+            self.graph = g
         return g
+
+    def input_views(self, packed):
+        """The step's inputs as views into a buffer in the packed layout."""
+        layout, total = self._input_layout()
+        if packed.numel() * packed.element_size() < total or packed.dtype != torch.uint8:
+            raise ValueError("packed input buffer: uint8 of at least %d bytes" % total)
+        return {name: packed[off:off + nb].view(dt).view(shape)
+                for name, off, shape, dt, nb in layout}
 
     def replay(self, cand, seq_lens, newest_slot, new_row, q):
         """One decode step through the captured graph (see `capture`)."""

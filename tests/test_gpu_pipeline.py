@@ -89,3 +89,51 @@ def test_full_hisparse_all_steps_sampled_attention():
     cfg = inputs.full_hisparse()
     rates = run_steps(cfg, cfg["pool"], attend_sample=[0, 63])
     assert rates[0] == 0.0 and min(rates[1:]) > 0.5
+
+
+def test_captured_step_matches_eager():
+    """The captured step, replayed with a staged copy of the inputs
+    (replay_packed) and as one graph per input slot read in place
+    (capture(slot=...)), gives the eager step's outputs and state bit for bit
+    at every step (the three decoders write identical BackUp rows into the
+    shared pool)."""
+    cfg = inputs.tiny_hisparse()
+    pool = cfg["pool"].pin_memory()
+    R = cfg["num_reqs"]
+
+    def make():
+        return HiSparseDecoder(host_pool=pool, block_table=torch.from_numpy(cfg["block_table"]),
+                               num_pages=cfg["num_pages"], page_size=cfg["page_size"],
+                               top_k=cfg["top_k"], hot_size=cfg["hot_size"],
+                               region_stride=cfg["region_stride"], heads=cfg["heads"],
+                               scale=cfg["scale"])
+
+    decs = [make(), make(), make()]
+    steps = []
+    for s in range(cfg["steps"]):
+        T = cfg["prefill"] + s + 1
+        seq = cuda(np.full(R, T, np.int32))
+        newest = decs[0].newest_slots(cuda(np.full(R, cfg["prefill"] + s, np.int32)), seq)
+        steps.append((cuda(cfg["cand"][s]), seq, newest, cfg["new_rows"][s].cuda(),
+                      cfg["q"][s].cuda()))
+    packed = [decs[0].pack_inputs(*st) for st in steps]
+    for d in decs:  # step 0 eagerly: the one-time set-up
+        d.step(*steps[0])
+    torch.cuda.synchronize()
+    decs[1].capture()
+    slot_graphs = [None] + [decs[2].capture(slot=packed[s]) for s in range(1, cfg["steps"])]
+    torch.cuda.synchronize()
+    for s in range(1, cfg["steps"]):
+        out0, lse0 = decs[0].step(*steps[s])
+        out1, lse1 = decs[1].replay_packed(packed[s])
+        out1, lse1 = out1.clone(), lse1.clone()
+        slot_graphs[s].replay()
+        torch.cuda.synchronize()
+        out2, lse2 = decs[2].out, decs[2].lse
+        for o, l in ((out1, lse1), (out2, lse2)):
+            assert torch.equal(o.view(torch.int16), out0.view(torch.int16)), f"step {s} out"
+            assert torch.equal(l, lse0), f"step {s} lse"
+        for d in decs[1:]:
+            for name in ("dgi", "lru", "stats", "hot"):
+                assert torch.equal(getattr(d, name), getattr(decs[0], name)), f"step {s} {name}"
+            assert d.status.item() == 0
