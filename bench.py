@@ -282,8 +282,9 @@ def run_full(args, rank, world, flush):
 def run_e2e(args, cfg, flush):
     """Same steps through the public API with the step's inputs in pinned host
     memory: every timed step copies its packed inputs (indices, lengths,
-    slots, new rows, q) host -> device into the captured step's input buffer
-    (one copy), replays the step and copies out + lse device -> host."""
+    slots, new rows, q) host -> device, runs the step and copies out + lse
+    device -> host, all as nodes of the step's captured graph (the index
+    inputs ahead of S1, q and the new rows beside S1 and S2)."""
     S = args.warmup + args.steps
     dec = make_decoder(cfg)
     dec.warm_pool()
@@ -301,16 +302,19 @@ def run_e2e(args, cfg, flush):
     dec.step(di_dev["cand"][0], di_dev["seq"][0], di_dev["newest"][0], di_dev["new_rows"][0],
              di_dev["q"][0], stream=stream)
     torch.cuda.synchronize()
-    dec.capture()
+    # One graph per step's pinned input buffer: the graph copies the inputs
+    # host -> device (indices ahead of S1, q and the new rows beside S1/S2)
+    # and the results device -> host as nodes of the step.
+    slot = torch.empty_like(host[0], device="cuda")
+    graphs = {s: dec.capture(slot=slot, host_in=host[s], host_out=(out_h, lse_h))
+              for s in range(1, S)}
     torch.cuda.synchronize()
     marks = []
     for s in range(1, S):
         flush_l2(flush)
         e0, e1 = ev(), ev()
         e0.record(stream)
-        out, lse = dec.replay_packed(host[s])
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        graphs[s].replay()
         e1.record(stream)
         if s >= args.warmup:
             marks.append((e0, e1))

@@ -80,7 +80,14 @@ def lib():
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device-visible address of a tensor argument: a CUDA tensor's own, or
+    the mapped address of a pinned host tensor (the kernels then read or
+    write host memory over the link)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        return ctypes.c_void_p(host_device_pointer(t))
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream=None):
@@ -101,8 +108,8 @@ def _check(t, dtype, name, cuda=True):
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
-    if cuda and not t.is_cuda:
-        raise ValueError(f"{name}: must be a CUDA tensor")
+    if cuda and not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name}: must be a CUDA tensor or pinned host memory")
 
 
 def status_string(code):
@@ -112,7 +119,7 @@ def status_string(code):
 def host_device_pointer(t):
     """Device-visible address of a pinned host tensor."""
     if not t.is_pinned():
-        raise ValueError("host pool must be pinned (pin_memory())")
+        raise ValueError("host memory must be pinned (pin_memory())")
     out = ctypes.c_void_p()
     _call("hs_host_device_pointer", ctypes.c_void_p(t.data_ptr()), ctypes.byref(out))
     return out.value

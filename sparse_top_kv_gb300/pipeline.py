@@ -77,6 +77,7 @@ class HiSparseDecoder:
         self.side = torch.cuda.Stream(device=dev)
         self.ev_lists = torch.cuda.Event()
         self.ev_attn = torch.cuda.Event()
+        self.ev_fork = torch.cuda.Event()
         # SMs left to the SwapIn while the resident-row attention runs (one
         # attention CTA per SM, one copy CTA per SM).
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -118,10 +119,15 @@ class HiSparseDecoder:
             num_pages=self.num_pages)
         return slot.view(-1).clone()
 
-    def step(self, cand, seq_lens, newest_slot, new_row, q, stream=None, events=None):
+    def step(self, cand, seq_lens, newest_slot, new_row, q, stream=None, events=None,
+             out=None, lse=None):
         """cand int32 [R, top_k] positions; seq_lens int32 [R]; newest_slot int32
         [R]; new_row [R, row_width] (the new token's KV row); q bf16 [R, H, d_qk].
         Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated.
+        cand, seq_lens and newest_slot may be pinned host tensors (the kernels
+        read them over the link); `out` / `lse`, if given (device or pinned
+        host tensors of those shapes), receive the results instead of the
+        decoder's own buffers.
 
         The SwapIn runs concurrently with the attention over the rows that
         were already resident (hit_idx, side stream); the attention over the
@@ -185,10 +191,12 @@ class HiSparseDecoder:
         hs.sparse_decode_finish(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                 miss_rows.view(R, 1, self.cap), miss_count.view(R, 1),
                                 self.scale, self.d_v, self.part_m, self.part_l, self.part_o,
-                                self.parts_hit, sync=self.sync, out=self.out, lse=self.lse,
+                                self.parts_hit, sync=self.sync,
+                                out=self.out if out is None else out,
+                                lse=self.lse if lse is None else lse,
                                 status=self.status, stream=main)
         rec(6, main)
-        return self.out, self.lse
+        return (self.out if out is None else out), (self.lse if lse is None else lse)
 
     def _input_layout(self):
         """Byte layout of one step's inputs packed in one buffer: (name,
@@ -218,7 +226,7 @@ class HiSparseDecoder:
             out[off:off + nbytes].view(dt).view(shape).copy_(t.reshape(shape))
         return out
 
-    def capture(self, events=None, slot=None):
+    def capture(self, events=None, slot=None, host_in=None, host_out=None):
         """Capture one decode step over static input buffers (`self.graph_in`,
         views of the packed buffer `self.graph_in_packed`) as a CUDA graph,
         both streams included.  `replay(...)` / `replay_packed(...)` then copy
@@ -232,7 +240,15 @@ class HiSparseDecoder:
         (`pack_inputs`) that the graph reads its inputs from in place: an
         engine that keeps each step's inputs in graph-stable slots (the model
         writes the next step's inputs into a slot) replays one such graph per
-        slot with no staging copy.  That graph is returned and not kept."""
+        slot with no staging copy.  That graph is returned and not kept.
+
+        `host_in`, if given, is a pinned host buffer in the packed layout:
+        S1, S2 and the BackUp read the index inputs (cand, seq, newest) from
+        it in place over the link, and the graph copies the new rows and q
+        into its device input buffer on the side stream, in parallel with S1
+        and S2 (they are first read after S2).  `host_out`, if given, is a
+        pair of pinned tensors (out, lse) that the finishing pass writes the
+        step's results into directly."""
         dev = self.device
         if slot is None:
             if getattr(self, "graph_in_packed", None) is None:
@@ -242,11 +258,24 @@ class HiSparseDecoder:
             gi = self.graph_in
         else:
             gi = self.input_views(slot)
+        dev_buf = self.graph_in_packed if slot is None else slot
         g = torch.cuda.CUDAGraph()
         self.side.wait_stream(torch.cuda.current_stream(dev))
+        idx = gi
+        if host_in is not None:
+            idx = self.input_views(host_in)
+        out, lse = (None, None) if host_out is None else host_out
         with torch.cuda.graph(g):
-            self.step(gi["cand"], gi["seq"], gi["newest"], gi["new_row"], gi["q"],
-                      events=events)
+            if host_in is not None:
+                main = torch.cuda.current_stream(dev)
+                layout, total = self._input_layout()
+                cut = dict((name, off) for name, off, _, _, _ in layout)["new_row"]
+                self.ev_fork.record(main)
+                self.side.wait_event(self.ev_fork)
+                with torch.cuda.stream(self.side):
+                    dev_buf[cut:total].copy_(host_in[cut:total], non_blocking=True)
+            self.step(idx["cand"], idx["seq"], idx["newest"], gi["new_row"], gi["q"],
+                      events=events, out=out, lse=lse)
         if slot is None:
             self.graph = g
         return g

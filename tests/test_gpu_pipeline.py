@@ -93,10 +93,11 @@ def test_full_hisparse_all_steps_sampled_attention():
 
 def test_captured_step_matches_eager():
     """The captured step, replayed with a staged copy of the inputs
-    (replay_packed) and as one graph per input slot read in place
-    (capture(slot=...)), gives the eager step's outputs and state bit for bit
-    at every step (the three decoders write identical BackUp rows into the
-    shared pool)."""
+    (replay_packed), as one graph per input slot read in place
+    (capture(slot=...)) and as one graph per pinned host input buffer with
+    the results copied back to pinned host tensors (host_in / host_out),
+    gives the eager step's outputs and state bit for bit at every step (the
+    decoders write identical BackUp rows into the shared pool)."""
     cfg = inputs.tiny_hisparse()
     pool = cfg["pool"].pin_memory()
     R = cfg["num_reqs"]
@@ -108,7 +109,7 @@ def test_captured_step_matches_eager():
                                region_stride=cfg["region_stride"], heads=cfg["heads"],
                                scale=cfg["scale"])
 
-    decs = [make(), make(), make()]
+    decs = [make(), make(), make(), make()]
     steps = []
     for s in range(cfg["steps"]):
         T = cfg["prefill"] + s + 1
@@ -122,15 +123,25 @@ def test_captured_step_matches_eager():
     torch.cuda.synchronize()
     decs[1].capture()
     slot_graphs = [None] + [decs[2].capture(slot=packed[s]) for s in range(1, cfg["steps"])]
+    # Inputs from pinned host buffers and results into pinned host tensors,
+    # both copied by the graph.
+    host_in = [p.cpu().pin_memory() for p in packed]
+    out_h = torch.empty(decs[3].out.shape, dtype=decs[3].out.dtype).pin_memory()
+    lse_h = torch.empty(decs[3].lse.shape, dtype=decs[3].lse.dtype).pin_memory()
+    dev_slot = torch.empty_like(packed[0])
+    host_graphs = [None] + [decs[3].capture(slot=dev_slot, host_in=host_in[s],
+                                            host_out=(out_h, lse_h))
+                            for s in range(1, cfg["steps"])]
     torch.cuda.synchronize()
     for s in range(1, cfg["steps"]):
         out0, lse0 = decs[0].step(*steps[s])
         out1, lse1 = decs[1].replay_packed(packed[s])
         out1, lse1 = out1.clone(), lse1.clone()
         slot_graphs[s].replay()
+        host_graphs[s].replay()
         torch.cuda.synchronize()
         out2, lse2 = decs[2].out, decs[2].lse
-        for o, l in ((out1, lse1), (out2, lse2)):
+        for o, l in ((out1, lse1), (out2, lse2), (out_h.cuda(), lse_h.cuda())):
             assert torch.equal(o.view(torch.int16), out0.view(torch.int16)), f"step {s} out"
             assert torch.equal(l, lse0), f"step {s} lse"
         for d in decs[1:]:
