@@ -35,8 +35,10 @@ def lib():
         L.hso_sparse_decode.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, i32, i32, i32,
                                         f64, P, P]
         L.hso_merge.argtypes = [P, P, P, i32, i32, i32, P, P, P]
+        L.hso_layer_transfer.argtypes = [P, P, i64, i64, i32, i32, i32, i32, i64, i64, P, P,
+                                         i32, i64, i32, P]
         for f in ("hso_normalize_indices", "hso_hot_lookup_assign", "hso_swap_in",
-                  "hso_backup", "hso_sparse_decode", "hso_merge"):
+                  "hso_backup", "hso_sparse_decode", "hso_merge", "hso_layer_transfer"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -141,6 +143,28 @@ def backup(src, src_rows, host_pool, dst_slots, row_bytes):
     rc = lib().hso_backup(_p(src), _p(src_rows), _p(host_pool), _p(dst_slots), len(dst_slots),
                           row_bytes, host_rows, _p(bad))
     _check(rc, "hso_backup")
+    return int(bad[0])
+
+
+def layer_transfer(dev, host, host_tokens, row_bytes, src_idx, dst_idx, *, page_size,
+                   page_first, direction):
+    """HiCache layer transfer.  dev: list over buffers of lists over layers of
+    uint8 arrays [dev_tokens * row_bytes] (updated in place for H2D); host:
+    uint8 array of nbuf pools of host_tokens * layers rows each (updated in
+    place for D2H); src_idx/dst_idx int32 or int64 [n].  Returns the number
+    of skipped (buffer, layer, row) copies."""
+    nbuf, layers = len(dev), len(dev[0])
+    dev_tokens = dev[0][0].size // row_bytes
+    ptrs = (ctypes.c_void_p * (nbuf * layers))(*[a.ctypes.data for bl in dev for a in bl])
+    src_idx = np.ascontiguousarray(src_idx)
+    dst_idx = np.ascontiguousarray(dst_idx, dtype=src_idx.dtype)
+    ib = src_idx.dtype.itemsize
+    bad = np.zeros(1, np.int64)
+    rc = lib().hso_layer_transfer(ctypes.cast(ptrs, ctypes.c_void_p), _p(host), host_tokens,
+                                  host_tokens * layers * row_bytes, nbuf, layers, page_size,
+                                  1 if page_first else 0, dev_tokens, row_bytes, _p(src_idx),
+                                  _p(dst_idx), ib, len(src_idx), direction, _p(bad))
+    _check(rc, "hso_layer_transfer")
     return int(bad[0])
 
 

@@ -273,6 +273,64 @@ int hso_backup(const uint8_t* src, const int64_t* src_rows, uint8_t* host_pool,
 }
 
 // ---------------------------------------------------------------------------
+// Layer transfer (SGLang PR "[HiCache] TMA-staged host<->device KV transfer
+// kernel (sm_90+)", Motivation and Modifications): HiCache moves the rows of
+// cached tokens between the pinned host pool and the device's per-layer
+// pools.  For every buffer b < nbuf (K and V, or one buffer for MLA), every
+// layer l < layers and every i < n, the row of token src_idx[i] is copied to
+// the row of token dst_idx[i].  Row addresses, in bytes:
+//   device pool (one array per buffer and layer): dev[b * layers + l] + t * rb
+//   host, layer-first:  host + b * host_buf_bytes + (l * host_tokens + t) * rb
+//   host, page-first:   host + b * host_buf_bytes
+//                       + ((t / P) * layers * P + l * P + t % P) * rb
+// direction 0 copies host -> device (src on the host), 1 device -> host.
+// Indices are int32 (index_bytes = 4) or int64 (8).  A source or destination
+// index outside its pool ([0, host_tokens) on the host, [0, dev_tokens) on the
+// device) skips the row; the number of skipped (buffer, layer, row) copies is
+// returned in *bad.
+int hso_layer_transfer(uint8_t* const* dev, uint8_t* host, int64_t host_tokens,
+                       int64_t host_buf_bytes, int32_t nbuf, int32_t layers, int32_t page_size,
+                       int32_t page_first, int64_t dev_tokens, int64_t row_bytes,
+                       const void* src_idx, const void* dst_idx, int32_t index_bytes, int64_t n,
+                       int32_t direction, int64_t* bad) {
+    if (row_bytes <= 0 || row_bytes % 16 != 0 || page_size <= 0) return 2;
+    if (index_bytes != 4 && index_bytes != 8) return 1;
+    const auto idx = [&](const void* p, int64_t i) -> int64_t {
+        return index_bytes == 4 ? static_cast<const int32_t*>(p)[i]
+                                : static_cast<const int64_t*>(p)[i];
+    };
+    const auto host_row = [&](int32_t b, int32_t l, int64_t t) -> uint8_t* {
+        int64_t r;
+        if (page_first) {
+            r = (t / page_size) * layers * page_size + static_cast<int64_t>(l) * page_size +
+                t % page_size;
+        } else {
+            r = static_cast<int64_t>(l) * host_tokens + t;
+        }
+        return host + b * host_buf_bytes + r * row_bytes;
+    };
+    *bad = 0;
+    for (int32_t b = 0; b < nbuf; ++b) {
+        for (int32_t l = 0; l < layers; ++l) {
+            uint8_t* dbase = dev[static_cast<int64_t>(b) * layers + l];
+            for (int64_t i = 0; i < n; ++i) {
+                const int64_t s = idx(src_idx, i), d = idx(dst_idx, i);
+                const int64_t s_lim = direction == 0 ? host_tokens : dev_tokens;
+                const int64_t d_lim = direction == 0 ? dev_tokens : host_tokens;
+                if (s < 0 || s >= s_lim || d < 0 || d >= d_lim) {
+                    *bad += 1;
+                    continue;
+                }
+                const uint8_t* from = direction == 0 ? host_row(b, l, s) : dbase + s * row_bytes;
+                uint8_t* to = direction == 0 ? dbase + d * row_bytes : host_row(b, l, d);
+                std::memcpy(to, from, static_cast<size_t>(row_bytes));
+            }
+        }
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
 // S4 -- sparse decode attention over the candidate rows ([PT] 3.1, 3.2, and
 // 7.3 "空集合": an empty set gives a zero output and LSE = -inf).
 //
