@@ -190,6 +190,42 @@ int hs_backup(const void* src, const int64_t* src_rows, void* host_pool,
               int32_t* status, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * hs_layer_transfer -- [HC] Motivation and Modifications: HiCache moves the
+ * rows of cached tokens between the pinned host pool and the device's
+ * per-layer pools, for every layer in one call (a pointer table), in either
+ * direction.  For every buffer b < nbuf (K and V, or one buffer for MLA),
+ * layer l < layers and i < n, the row of token src_idx[i] is copied to the
+ * row of token dst_idx[i].  Rows are row_bytes long (a multiple of 16, at
+ * most 8192).
+ *
+ * dev_layers  device array [nbuf * layers] (at most 4096) of device pointers: the pool of
+ *             buffer b and layer l is dev_layers[b * layers + l], rows of
+ *             token t at + t * row_bytes (16-byte aligned pools).
+ * host_pool   device-visible address of the pinned host pool; buffer b
+ *             starts host_buf_bytes * b into it (>= host_tokens * layers *
+ *             row_bytes when nbuf > 1).  page_first = 0: token t of layer l
+ *             at row l * host_tokens + t; page_first = 1: at row
+ *             ((t / page_size) * layers + l) * page_size + t % page_size (a
+ *             page's rows of one layer are contiguous; host_tokens is then a
+ *             multiple of page_size).
+ * src_idx, dst_idx  device arrays of n int32 (index_bytes 4) or int64 (8)
+ *             token ids; the same ids serve every buffer and layer.
+ * direction   0: host -> device (src ids on the host), 1: device -> host.
+ * max_ctas    SMs the copy may occupy, one CTA each (0 = every SM).
+ * status      int32 device word or NULL: an id outside its pool ([0,
+ *             host_tokens) on the host side, [0, dev_tokens) on the device
+ *             side) skips that row and stores HS_ERR_BAD_INDEX.
+ * Staged through shared-memory rings: consecutive ids whose rows are one
+ * contiguous run on both sides (whole pages) are one bulk copy; scattered
+ * rows are 16-byte copies by whole warps.
+ * ------------------------------------------------------------------------- */
+int hs_layer_transfer(void* const* dev_layers, void* host_pool, int64_t host_tokens,
+                      int64_t host_buf_bytes, int32_t nbuf, int32_t layers, int32_t page_size,
+                      int32_t page_first, int64_t dev_tokens, int64_t row_bytes,
+                      const void* src_idx, const void* dst_idx, int32_t index_bytes, int64_t n,
+                      int32_t direction, int32_t max_ctas, int32_t* status, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * S4  hs_sparse_decode -- [PT] 3.1 eqs. (4)-(6) (online softmax over tiles of
  * the candidate set), 3.2 (mask before the exponent; an empty set gives a
  * zero output and LSE = -inf) and eq. (7) (split-KV merge); [PA] 1.4 (GQA:

@@ -62,11 +62,20 @@ struct XferArgs {
     int32_t* status;
     uint64_t timeout_ns;
     int32_t* ticket;        // [2] claim and exit counters (zero on entry, left zero), or nullptr
+    // Layer transfer: list r is (buffer r / layers, layer r % layers), every
+    // list reads the same index arrays, and row addresses follow the pools'
+    // layouts instead of base + id * row_bytes.
+    int32_t layer_mode;
+    int32_t layers, page_first, page_size, page_shift;  // page_shift = log2(page_size) or -1
+    int32_t to_host;             // 1: device pools -> host pool, 0: host -> device
+    uint8_t* const* dev_layers;  // device array [nbuf * layers] of per-layer pools
+    uint8_t* host_base;          // device-visible host pool: nbuf pools of host_buf_bytes
+    int64_t host_tokens, host_buf_bytes;
 };
 
 struct WarpRing {
     uint64_t full[kWS];
-    int64_t dst[kWS][kMaxGroup];  // destination row of each staged row, -1 = none
+    int64_t dst[kWS][kMaxGroup];  // destination address of each staged row, -1 = none
 };
 
 constexpr size_t kRingBytes = size_t(kWarps) * kWS * kStageBytes;
@@ -74,6 +83,32 @@ constexpr size_t kRingBytes = size_t(kWarps) * kWS * kStageBytes;
 __device__ __forceinline__ int64_t list_count(const XferArgs& a, int r) {
     const int64_t c = a.counts ? int64_t(a.counts[r]) : int64_t(a.fixed_count);
     return c < 0 ? 0 : (c > a.list_stride ? a.list_stride : c);
+}
+
+// Row t of the host pool for buffer b and layer l: page-first pools hold the
+// layers' rows of one page next to each other ([page][layer][token in page]),
+// layer-first pools one layer after the other ([layer][token]).
+__device__ __forceinline__ uint8_t* host_row(const XferArgs& a, int b, int l, int64_t t) {
+    int64_t r;
+    if (a.page_first) {
+        const int64_t pg = a.page_shift >= 0 ? (t >> a.page_shift) : t / a.page_size;
+        r = (pg * a.layers + l) * a.page_size + (t - pg * a.page_size);
+    } else {
+        r = int64_t(l) * a.host_tokens + t;
+    }
+    return a.host_base + int64_t(b) * a.host_buf_bytes + r * a.row_bytes;
+}
+
+// Addresses of source row `id` and destination row `id` of list r.
+__device__ __forceinline__ const uint8_t* src_row(const XferArgs& a, int r, int64_t id) {
+    if (!a.layer_mode) return a.src_base + id * a.row_bytes;
+    if (a.to_host) return a.dev_layers[r] + id * a.row_bytes;
+    return host_row(a, r / a.layers, r % a.layers, id);
+}
+__device__ __forceinline__ uint8_t* dst_row(const XferArgs& a, int r, int64_t id) {
+    if (!a.layer_mode) return a.dst_base + id * a.row_bytes;
+    if (a.to_host) return host_row(a, r / a.layers, r % a.layers, id);
+    return a.dev_layers[r] + id * a.row_bytes;
 }
 
 // Writes one landed stage out: the warp's lanes copy 16-byte vectors from
@@ -85,7 +120,7 @@ __device__ __forceinline__ void store_group(const XferArgs& a, const WarpRing& R
         const int64_t d = R.dst[st][k];
         if (d < 0) continue;
         const uint4* src = reinterpret_cast<const uint4*>(stage + int64_t(k) * rb);
-        uint4* dst = reinterpret_cast<uint4*>(a.dst_base + d * rb);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uintptr_t>(d));
         for (int v = lane; v < nv; v += 32) dst[v] = src[v];
     }
 }
@@ -150,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
             const int r = lo;
             const int64_t m0 = int64_t(gidx - prefix[r]) * a.group;
             const int nrows = int(hs::min64(list_count(a, r), m0 + a.group) - m0);
-            const int64_t off = int64_t(r) * a.list_stride + m0;
+            const int64_t off = (a.layer_mode ? 0 : int64_t(r) * a.list_stride) + m0;
             int64_t g = -1, d = -1;
             if (lane < nrows) {
                 g = a.src32 ? int64_t(a.src32[off + lane]) : a.src64[off + lane];
@@ -159,6 +194,12 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
             const bool src_ok = g >= 0 && (a.src_limit < 0 || g < a.src_limit);
             const bool dst_ok = d >= 0 && (a.dst_limit < 0 || d < a.dst_limit);
             bool copy = lane < nrows && src_ok && dst_ok;
+            // Row addresses (as integers, so that they shuffle and compare).
+            int64_t sp = -1, dp = -1;
+            if (copy) {
+                sp = int64_t(reinterpret_cast<uintptr_t>(src_row(a, r, g)));
+                dp = int64_t(reinterpret_cast<uintptr_t>(dst_row(a, r, d)));
+            }
             if (lane < nrows && !dst_ok) bad = true;
             if (lane < nrows && dst_ok && !src_ok && (!a.zero_bad_src || a.dgi == nullptr))
                 bad = true;
@@ -169,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 const int k = __ffs(zmask) - 1;
                 zmask &= zmask - 1;
                 const int64_t dk = __shfl_sync(0xffffffffu, d, k);
-                uint4* z = reinterpret_cast<uint4*>(a.dst_base + dk * rb);
+                uint4* z = reinterpret_cast<uint4*>(dst_row(a, r, dk));
                 for (int v = lane; v < nv; v += 32) z[v] = make_uint4(0, 0, 0, 0);
                 if (lane == 0 && a.dgi != nullptr) {
                     const int64_t s = dk - int64_t(r) * a.region_stride;
@@ -179,13 +220,15 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
             // The stage's previous group was written out (synchronously) at
             // an earlier iteration by every lane of this warp.
             __syncwarp();
-            if (lane < kMaxGroup) R.dst[st][lane] = copy ? d : int64_t(-1);
+            if (lane < kMaxGroup) R.dst[st][lane] = copy ? dp : int64_t(-1);
             const unsigned cmask = __ballot_sync(0xffffffffu, copy);
-            // One contiguous run of valid rows (source and destination) -> one
-            // bulk op; otherwise 16-byte copies by the whole warp.
-            const int64_t g0 = __shfl_sync(0xffffffffu, g, 0);
-            const int64_t d0 = __shfl_sync(0xffffffffu, d, 0);
-            const bool in_run = !(lane < nrows) || (copy && g == g0 + lane && d == d0 + lane);
+            // One contiguous run of valid rows (source and destination
+            // addresses) -> one bulk op; otherwise 16-byte copies by the whole
+            // warp.
+            const int64_t sp0 = __shfl_sync(0xffffffffu, sp, 0);
+            const int64_t dp0 = __shfl_sync(0xffffffffu, dp, 0);
+            const bool in_run = !(lane < nrows) ||
+                                (copy && sp == sp0 + lane * rb && dp == dp0 + lane * rb);
             const bool one_run = nrows > 1 && cmask == ((nrows == 32) ? 0xffffffffu : ((1u << nrows) - 1u)) &&
                                  __all_sync(0xffffffffu, in_run);
             __syncwarp();
@@ -193,7 +236,8 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 if (lane == 0) {
                     const uint32_t bytes = uint32_t(nrows * rb);
                     hs::mbar_arrive_expect_tx(&R.full[st], bytes);
-                    hs::bulk_g2s(stage, a.src_base + g0 * rb, bytes, &R.full[st]);
+                    hs::bulk_g2s(stage, reinterpret_cast<const void*>(static_cast<uintptr_t>(sp0)),
+                                 bytes, &R.full[st]);
                 } else {
                     hs::mbar_arrive(&R.full[st]);
                 }
@@ -202,8 +246,9 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 while (m) {
                     const int k = __ffs(m) - 1;
                     m &= m - 1;
-                    const int64_t gk = __shfl_sync(0xffffffffu, g, k);
-                    const unsigned char* src = a.src_base + gk * rb;
+                    const int64_t spk = __shfl_sync(0xffffffffu, sp, k);
+                    const unsigned char* src =
+                        reinterpret_cast<const unsigned char*>(static_cast<uintptr_t>(spk));
                     const uint32_t dsm = hs::smem_u32(stage + int64_t(k) * rb);
                     for (int v = lane; v < nv; v += 32)
                         hs::tc_cp_async16(dsm + v * 16, src + v * 16);
@@ -327,4 +372,61 @@ extern "C" int hs_backup(const void* src, const int64_t* src_rows, void* host_po
     a.status = status;
     a.timeout_ns = hs::kWaitTimeoutNs;
     return launch_xfer(a, n, 0, stream);
+}
+
+extern "C" int hs_layer_transfer(void* const* dev_layers, void* host_pool, int64_t host_tokens,
+                                 int64_t host_buf_bytes, int32_t nbuf, int32_t layers,
+                                 int32_t page_size, int32_t page_first, int64_t dev_tokens,
+                                 int64_t row_bytes, const void* src_idx, const void* dst_idx,
+                                 int32_t index_bytes, int64_t n, int32_t direction,
+                                 int32_t max_ctas, int32_t* status, hs_stream_t stream) {
+    if (nbuf <= 0 || layers <= 0 || page_size <= 0 || host_tokens < 0 || dev_tokens < 0 ||
+        n < 0 || n > INT32_MAX || max_ctas < 0 || row_bytes <= 0 ||
+        (direction != 0 && direction != 1) || (index_bytes != 4 && index_bytes != 8) ||
+        int64_t(nbuf) * layers > 4096)
+        return HS_ERR_INVALID_ARG;
+    if (row_bytes % 16 != 0 || host_buf_bytes % 16 != 0) return HS_ERR_MISALIGNED;
+    if (row_bytes > int64_t(kStageBytes)) return HS_ERR_CAPACITY;
+    if (page_first && host_tokens % page_size != 0) return HS_ERR_INVALID_ARG;
+    if (host_buf_bytes < host_tokens * int64_t(layers) * row_bytes && nbuf > 1)
+        return HS_ERR_INVALID_ARG;
+    if (n == 0) return HS_OK;
+    if (dev_layers == nullptr || host_pool == nullptr || src_idx == nullptr ||
+        dst_idx == nullptr)
+        return HS_ERR_INVALID_ARG;
+    if (!aligned16(host_pool)) return HS_ERR_MISALIGNED;
+    XferArgs a{};
+    a.row_bytes = row_bytes;
+    a.to_host = direction;
+    a.src_limit = direction == 0 ? host_tokens : dev_tokens;
+    a.dst_limit = direction == 0 ? dev_tokens : host_tokens;
+    if (index_bytes == 4) {
+        a.src32 = static_cast<const int32_t*>(src_idx);
+        a.dst32 = static_cast<const int32_t*>(dst_idx);
+    } else {
+        a.src64 = static_cast<const int64_t*>(src_idx);
+        a.dst64 = static_cast<const int64_t*>(dst_idx);
+    }
+    a.counts = nullptr;
+    a.fixed_count = int32_t(n);
+    a.nlists = nbuf * layers;
+    a.list_stride = int32_t(n);
+    a.zero_bad_src = 0;
+    a.status = status;
+    a.timeout_ns = hs::kWaitTimeoutNs;
+    a.layer_mode = 1;
+    a.layers = layers;
+    a.page_first = page_first ? 1 : 0;
+    a.page_size = page_size;
+    a.page_shift = -1;
+    if ((page_size & (page_size - 1)) == 0) {
+        int sh = 0;
+        while ((1 << sh) < page_size) ++sh;
+        a.page_shift = sh;
+    }
+    a.dev_layers = reinterpret_cast<uint8_t* const*>(dev_layers);
+    a.host_base = static_cast<uint8_t*>(host_pool);
+    a.host_tokens = host_tokens;
+    a.host_buf_bytes = host_buf_bytes;
+    return launch_xfer(a, int64_t(a.nlists) * n, max_ctas, stream);
 }

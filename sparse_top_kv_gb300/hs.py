@@ -38,6 +38,8 @@ _SIGS = {
     "hs_hot_state_reset": ([_P, _P, _I32, _I32, _P], ctypes.c_int),
     "hs_hot_lookup_assign": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
                               _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "hs_layer_transfer": ([_P, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I64, _I64, _P, _P, _I32,
+                           _I64, _I32, _I32, _P, _P], ctypes.c_int),
     "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _I32, _P, _P, _P],
                    ctypes.c_int),
     "hs_backup": ([_P, _P, _P, _P, _I32, _I64, _I64, _P, _P], ctypes.c_int),
@@ -211,6 +213,39 @@ def swap_in(host_pool_dev, host_rows, hot, row_bytes, miss_src, miss_dst, miss_c
     _call("hs_swap_in", ctypes.c_void_p(host_pool_dev), host_rows, _ptr(hot), row_bytes,
           _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), rows, cap, _ptr(dgi), hot_size,
           region_stride, max_ctas, _ptr(ticket), _ptr(status), _stream(stream))
+
+
+def layer_pointer_table(dev_pools):
+    """Device pointer table for layer_transfer: dev_pools is a list over
+    buffers (K, V; or one for MLA) of lists over layers of CUDA tensors
+    [dev_tokens, ...] (row-major rows).  Build it once, outside graph capture."""
+    ptrs = [t.data_ptr() for pools in dev_pools for t in pools]
+    return torch.tensor(ptrs, dtype=torch.int64, device=dev_pools[0][0].device)
+
+
+def layer_transfer(table, nbuf, layers, dev_tokens, row_bytes, host_pool, host_tokens,
+                   src_idx, dst_idx, *, page_size, page_first, direction, max_ctas=0,
+                   status=None, stream=None):
+    """HiCache layer transfer (see hs_layer_transfer): table from
+    layer_pointer_table; host_pool a pinned host tensor holding nbuf pools of
+    host_tokens * layers rows; src_idx/dst_idx int32 or int64 CUDA tensors [n];
+    direction 0 host -> device, 1 device -> host."""
+    _check(table, torch.int64, "table")
+    if src_idx.dtype not in (torch.int32, torch.int64) or dst_idx.dtype != src_idx.dtype:
+        raise TypeError("src_idx/dst_idx: int32 or int64, the same dtype")
+    _check(src_idx, src_idx.dtype, "src_idx")
+    _check(dst_idx, dst_idx.dtype, "dst_idx")
+    _check(status, torch.int32, "status")
+    if table.numel() != nbuf * layers:
+        raise ValueError("table holds nbuf * layers pointers")
+    n = src_idx.numel()
+    if dst_idx.numel() != n:
+        raise ValueError("src_idx and dst_idx differ in length")
+    hdev = host_device_pointer(host_pool)
+    _call("hs_layer_transfer", _ptr(table), ctypes.c_void_p(hdev), host_tokens,
+          host_tokens * layers * row_bytes, nbuf, layers, page_size, 1 if page_first else 0,
+          dev_tokens, row_bytes, _ptr(src_idx), _ptr(dst_idx), src_idx.element_size(), n,
+          direction, max_ctas, _ptr(status), _stream(stream))
 
 
 def backup(src, src_rows, host_pool_dev, dst_slots, row_bytes, host_rows, *, status=None,

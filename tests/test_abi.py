@@ -53,6 +53,17 @@ def test_host_side_argument_checks():
     assert L.hs_swap_in(P, 10, P, 100, P, P, P, 1, 1, P, 0, 0, 0, P, P, P) == 2
     assert L.hs_swap_in(P, 10, P, 96, P, P, P, 1, 1, P, 0, 0, -1, P, P, P) == 1
     assert L.hs_backup(P, P, P, P, 1, 24, 10, P, P) == 2
+    # Layer transfer: rows not a multiple of 16, index width, direction,
+    # too many layers, a page-first pool that is not whole pages.
+    assert L.hs_layer_transfer(P, P, 64, 0, 1, 1, 16, 0, 64, 100, P, P, 4, 1, 0, 0, P,
+                               P) == 2
+    assert L.hs_layer_transfer(P, P, 64, 0, 1, 1, 16, 0, 64, 96, P, P, 2, 1, 0, 0, P, P) == 1
+    assert L.hs_layer_transfer(P, P, 64, 0, 1, 1, 16, 0, 64, 96, P, P, 4, 1, 2, 0, P, P) == 1
+    assert L.hs_layer_transfer(P, P, 64, 0, 2, 4000, 16, 0, 64, 96, P, P, 4, 1, 0, 0, P,
+                               P) == 1
+    assert L.hs_layer_transfer(P, P, 60, 0, 1, 1, 16, 1, 64, 96, P, P, 4, 1, 0, 0, P, P) == 1
+    assert L.hs_layer_transfer(P, P, 64, 0, 1, 1, 16, 0, 64, 16384, P, P, 4, 1, 0, 0, P,
+                               P) == 3
     # Unsupported attention shape, null pointers.
     buf = ctypes.create_string_buffer(4096)
     p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 16), ctypes.c_void_p)
