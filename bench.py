@@ -415,6 +415,62 @@ def bench_swapin(reps=10):
     return res
 
 
+def bench_hicache(reps=10):
+    """HiCache layer transfer: K and V rows of 512 B (4 KV heads x 64 bf16),
+    128-token pages, 32768 tokens (256 random pages of a 65536-token pool),
+    4 layers in one call; host -> device from a page-first host pool and
+    device -> host into a layer-first one, on 4 SMs and on every SM, against a
+    pinned cudaMemcpyAsync of the same byte count."""
+    cfg = inputs.hicache()
+    nbuf, layers, P, rb = cfg["nbuf"], cfg["layers"], cfg["page_size"], cfg["row_bytes"]
+    host_tokens, n, host = cfg["host_tokens"], cfg["n"], cfg["pool"]
+    dev = [[torch.empty(n, rb, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+           for _ in range(nbuf)]
+    table = hs.layer_pointer_table(dev)
+    src = torch.from_numpy(cfg["tokens"]).cuda()
+    dst = torch.arange(n, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nbytes = nbuf * layers * n * rb
+    res = {"workload": "hicache: K+V rows of 512 B, 4 layers, 128-token pages, 32768 tokens "
+                       "(256 pages of a 65536-token pool), one call for all layers",
+           "bytes": nbytes}
+
+    def timed(fn):
+        tt = []
+        for i in range(reps + 3):
+            a, b = ev(), ev()
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            if i >= 3:
+                tt.append(a.elapsed_time(b))
+        return statistics.median(tt)
+
+    for name, direction, page_first, s_idx, d_idx in (("h2d_page_first_host", 0, True, src, dst),
+                                                     ("d2h_layer_first_host", 1, False, dst, src)):
+        r = {}
+        for ctas in (4, 0):
+            ms = timed(lambda: hs.layer_transfer(table, nbuf, layers, n, rb, host, host_tokens,
+                                                 s_idx, d_idx, page_size=P,
+                                                 page_first=page_first, direction=direction,
+                                                 max_ctas=ctas, status=status))
+            r["gbs_4sm" if ctas == 4 else "gbs_all_sm"] = nbytes / ms / 1e6
+        big = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        hsrc = host[:nbytes]
+        if direction == 0:
+            ms = timed(lambda: big.copy_(hsrc, non_blocking=True))
+        else:
+            ms = timed(lambda: hsrc.copy_(big, non_blocking=True))
+        r["ceiling_memcpy_gbs"] = nbytes / ms / 1e6
+        r["frac_of_ceiling_all_sm"] = r["gbs_all_sm"] / r["ceiling_memcpy_gbs"]
+        res[name] = r
+        del big
+    assert int(status.item()) == 0, f"device status {status.item()}"
+    del dev, host
+    return res
+
+
 def bench_mla_decode(hbm_peak, flush, reps=20):
     cfg = inputs.mla_decode()
     R, H = cfg["num_reqs"], cfg["heads"]
@@ -706,6 +762,8 @@ def main():
         extras["mla_decode"] = bench_mla_decode(hbm_peak, flush)
         torch.cuda.empty_cache()
         extras["gqa_union"] = bench_gqa(hbm_peak, flush)
+        torch.cuda.empty_cache()
+        extras["hicache"] = bench_hicache()
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -35,7 +35,8 @@ import math
 import numpy as np
 import torch
 
-SEEDS = {"tiny_hisparse": 0, "swapin": 1, "mla_decode": 2, "full_hisparse": 3, "gqa_union": 4}
+SEEDS = {"tiny_hisparse": 0, "swapin": 1, "mla_decode": 2, "full_hisparse": 3, "gqa_union": 4,
+         "hicache": 5}
 
 
 def _rng(seed):
@@ -260,3 +261,25 @@ def gqa_union(num_reqs=16, heads=32, kv_heads=8, d=128, ctx=65536, page=16, n_un
     cfg["cand"] = cand
     cfg["row_req"] = np.repeat(np.arange(num_reqs, dtype=np.int32), kv_heads)
     return cfg
+
+
+def hicache(nbuf=2, layers=4, page_size=128, row_bytes=512, host_tokens=65536, n=32768):
+    """HiCache layer-transfer workload (K and V rows of 512 B = 4 KV heads x 64
+    bf16, 128-token pages): a pinned host pool of random bytes holding nbuf
+    pools of host_tokens * layers rows, and n // page_size whole random pages
+    (sorted) as the token ids to move."""
+    seed = SEEDS["hicache"]
+    rng = _rng(seed)
+    pool = pinned_empty((nbuf * layers * host_tokens * row_bytes,), torch.uint8)
+    chunk = 1 << 24
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    for o in range(0, pool.numel(), chunk):
+        e = min(pool.numel(), o + chunk)
+        pool[o:e].copy_(torch.randint(0, 256, (e - o,), generator=g, device="cuda",
+                                      dtype=torch.uint8))
+    torch.cuda.synchronize()
+    host_read_pass(pool)
+    pg = np.sort(rng.choice(host_tokens // page_size, size=n // page_size, replace=False))
+    tokens = (pg[:, None] * page_size + np.arange(page_size)[None]).reshape(-1).astype(np.int64)
+    return dict(name="hicache", pool=pool, tokens=tokens, nbuf=nbuf, layers=layers,
+                page_size=page_size, row_bytes=row_bytes, host_tokens=host_tokens, n=n)
