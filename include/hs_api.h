@@ -182,8 +182,10 @@ int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, int64_t row_
  * hs_backup -- [HS] overview "BackUp": after each step copy the newly
  * generated KV row to host memory.  host_pool[dst_slots[i]] := src[src_rows[i]]
  * for i < n.  src is a device buffer of rows of row_bytes; src_rows int64 [n]
- * and dst_slots int32 [n] are device arrays.  A destination outside
- * [0, host_rows) is skipped and reported as HS_ERR_BAD_INDEX in *status.
+ * and dst_slots int32 [n] are device arrays.  A destination of -1 is padding
+ * (an inactive request of a fixed-size batch) and is skipped; any other
+ * destination outside [0, host_rows) is skipped and reported as
+ * HS_ERR_BAD_INDEX in *status.
  * ------------------------------------------------------------------------- */
 int hs_backup(const void* src, const int64_t* src_rows, void* host_pool,
               const int32_t* dst_slots, int32_t n, int64_t row_bytes, int64_t host_rows,

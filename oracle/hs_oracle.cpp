@@ -256,8 +256,10 @@ int hso_swap_in(const uint8_t* host_pool, int64_t host_rows, uint8_t* hot, int64
 }
 
 // BackUp ([HS] overview: "BackUp" copies each step's new KV row to host
-// memory): host_pool[dst_slots[i]] = src[src_rows[i]].  A destination outside
-// [0, host_rows) is not written; the number of such rows is returned in *bad.
+// memory): host_pool[dst_slots[i]] = src[src_rows[i]].  A destination of -1
+// is padding (an inactive request of a fixed-size batch) and is skipped; any
+// other destination outside [0, host_rows) is not written either, and the
+// number of those rows is returned in *bad.
 int hso_backup(const uint8_t* src, const int64_t* src_rows, uint8_t* host_pool,
                const int32_t* dst_slots, int32_t n, int64_t row_bytes, int64_t host_rows,
                int32_t* bad) {
@@ -265,6 +267,7 @@ int hso_backup(const uint8_t* src, const int64_t* src_rows, uint8_t* host_pool,
     *bad = 0;
     for (int32_t i = 0; i < n; ++i) {
         const int64_t g = dst_slots[i];
+        if (g == -1) continue;
         if (g < 0 || g >= host_rows) { *bad += 1; continue; }
         std::memcpy(host_pool + g * row_bytes, src + src_rows[i] * row_bytes,
                     static_cast<size_t>(row_bytes));

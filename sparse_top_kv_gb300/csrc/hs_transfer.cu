@@ -57,6 +57,7 @@ struct XferArgs {
     int32_t group;          // rows per group (<= kMaxGroup, group * row_bytes <= kStageBytes)
     int32_t* dgi;           // swap-in revocation target, or nullptr
     int32_t zero_bad_src;   // 1: a missing source zeroes the destination (SwapIn)
+    int32_t pad_dst;        // 1: a destination id of -1 is padding, skipped silently (BackUp)
     int32_t hot_size;
     int64_t region_stride;
     int32_t* status;
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 sp = int64_t(reinterpret_cast<uintptr_t>(src_row(a, r, g)));
                 dp = int64_t(reinterpret_cast<uintptr_t>(dst_row(a, r, d)));
             }
-            if (lane < nrows && !dst_ok) bad = true;
+            if (lane < nrows && !dst_ok && !(a.pad_dst && d == -1)) bad = true;
             if (lane < nrows && dst_ok && !src_ok && (!a.zero_bad_src || a.dgi == nullptr))
                 bad = true;
             // Rows without a source: zero the destination and revoke the slot.
@@ -365,6 +366,7 @@ extern "C" int hs_backup(const void* src, const int64_t* src_rows, void* host_po
     a.dst_limit = host_rows;
     a.src64 = src_rows;
     a.dst32 = dst_slots;
+    a.pad_dst = 1;
     a.counts = nullptr;
     a.fixed_count = n;
     a.nlists = 1;

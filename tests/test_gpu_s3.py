@@ -122,3 +122,20 @@ def test_swapin_config_full_size():
     torch.cuda.synchronize()
     assert status.item() == 0
     np.testing.assert_array_equal(pool.numpy(), ref)
+
+
+def test_backup_padding_destination():
+    """-1 destinations (inactive requests) are skipped without an error."""
+    rb = 1152
+    pool = torch.zeros(100, rb, dtype=torch.uint8).pin_memory()
+    src = cuda(np.random.default_rng(4).integers(1, 256, size=(8, rb), dtype=np.uint8))
+    src_rows = np.array([1, 2, 3, 4], np.int64)
+    dst = np.array([-1, 7, -1, 60], np.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = pool.numpy().copy()
+    bad = oracle.backup(u8(src).reshape(-1), src_rows, ref.reshape(-1), dst, rb)
+    hs.backup(src, cuda(src_rows), hs.host_device_pointer(pool), cuda(dst), rb, 100,
+              status=status)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(pool.numpy(), ref)
+    assert bad == 0 and status.item() == 0

@@ -74,3 +74,17 @@ def test_backup():
     assert bad == 1
     assert (host[3] == src[9]).all() and (host[11] == src[0]).all()
     assert (np.delete(host, [3, 11], axis=0) == 0).all()
+
+
+def test_backup_padding_destination():
+    """A destination of -1 is padding (an inactive request of a fixed-size
+    batch): nothing is written and nothing is counted; -2 is still an error."""
+    rng = np.random.default_rng(5)
+    rb = 32
+    src = rng.integers(1, 256, size=(6, rb), dtype=np.uint8)
+    host = np.zeros((8, rb), np.uint8)
+    bad = oracle.backup(src.reshape(-1), np.array([0, 1, 2, 3]), host.reshape(-1),
+                        np.array([-1, 5, -1, -2]), rb)
+    assert bad == 1
+    assert (host[5] == src[1]).all()
+    assert (np.delete(host, [5], axis=0) == 0).all()
