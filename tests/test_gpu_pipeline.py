@@ -148,3 +148,63 @@ def test_captured_step_matches_eager():
             for name in ("dgi", "lru", "stats", "hot"):
                 assert torch.equal(getattr(d, name), getattr(decs[0], name)), f"step {s} {name}"
             assert d.status.item() == 0
+
+
+def test_inactive_requests_in_a_captured_step():
+    """Graph-stable stepping with a changing set of active requests: one
+    captured step serves every step of a fixed-size batch; an inactive
+    request's row is padding (no candidates, context length 0, newest slot
+    -1).  Every step is compared with the oracle's step on the same inputs;
+    an inactive request gets a zero output and LSE -inf and keeps its dgi and
+    lru."""
+    cfg = inputs.full_hisparse(steps=6, num_reqs=4, top_k=256)
+    pool = cfg["pool"]
+    R, B, rb = cfg["num_reqs"], cfg["page_size"], 576 * 2
+    dec = HiSparseDecoder(host_pool=pool, block_table=torch.from_numpy(cfg["block_table"]),
+                          num_pages=cfg["num_pages"], page_size=B, top_k=cfg["top_k"],
+                          hot_size=cfg["hot_size"], region_stride=cfg["region_stride"],
+                          heads=cfg["heads"], scale=cfg["scale"])
+    ora = OracleHiSparse(host_pool_u8=pool.view(torch.uint8).numpy(),
+                         block_table=cfg["block_table"], num_pages=cfg["num_pages"],
+                         page_size=B, top_k=cfg["top_k"], hot_size=cfg["hot_size"],
+                         region_stride=cfg["region_stride"], row_bytes=rb, scale=cfg["scale"])
+    active = [[1, 1, 1, 1], [1, 0, 1, 1], [0, 1, 1, 0], [1, 1, 0, 1], [1, 1, 1, 1], [0, 0, 1, 1]]
+    for s in range(cfg["steps"]):
+        act = np.array(active[s], bool)
+        T = cfg["prefill"] + s + 1
+        seq = np.where(act, T, 0).astype(np.int32)
+        newest_pos = np.where(act, cfg["prefill"] + s, -1).astype(np.int32)
+        cand = cfg["cand"][s].copy()
+        cand[~act] = -1
+        g_newest = dec.newest_slots(cuda(newest_pos), cuda(seq))
+        o_newest = ora.newest_slots(newest_pos, seq)
+        np.testing.assert_array_equal(np_i32(g_newest), o_newest)
+        assert (o_newest[~act] == -1).all()
+        q, new_row = cfg["q"][s], cfg["new_rows"][s]
+        dgi0, lru0 = np_i32(dec.dgi).copy(), np_i32(dec.lru).copy()
+        if s == 0:  # the eager first step performs the one-time set-up
+            out, lse = dec.step(cuda(cand), cuda(seq), g_newest, new_row.cuda(), q.cuda())
+            dec.capture()
+        else:
+            out, lse = dec.replay_packed(dec.pack_inputs(cuda(cand), cuda(seq), g_newest,
+                                                         new_row.cuda(), q.cuda()))
+        torch.cuda.synchronize()
+        ref = ora.step(cand, seq, o_newest, u8(new_row).reshape(R, rb), bits(q))
+        tok, slot, count, err = dec.s1_out
+        for name, g in (("tok", tok), ("slot", slot), ("count", count), ("err", err)):
+            np.testing.assert_array_equal(np_i32(g), ref[name], err_msg=f"step {s} {name}")
+        hot_idx, mm, msrc, mdst, mcount = dec.s2_out[:5]
+        for name, g in (("hot_idx", hot_idx), ("miss_mask", mm), ("miss_count", mcount)):
+            np.testing.assert_array_equal(np_i32(g), ref[name], err_msg=f"step {s} {name}")
+        np.testing.assert_array_equal(np_i32(dec.dgi), ora.dgi, err_msg=f"step {s} dgi")
+        np.testing.assert_array_equal(np_i32(dec.lru), ora.lru, err_msg=f"step {s} lru")
+        np.testing.assert_array_equal(u8(dec.hot), ora.hot, err_msg=f"step {s} hot bytes")
+        assert dec.status.item() == 0 and ref["backup_bad"] == 0
+        for r in np.flatnonzero(~act):
+            np.testing.assert_array_equal(np_i32(dec.dgi)[r], dgi0[r])
+            np.testing.assert_array_equal(np_i32(dec.lru)[r], lru0[r])
+            assert int(np_i32(count)[r]) == 0
+            assert not out[r].float().abs().sum().item()
+            assert torch.isinf(lse[r]).all() and (lse[r] < 0).all()
+        rows = torch.from_numpy(np.flatnonzero(act)).cuda()
+        check_attention(out[rows], lse[rows], ref["out"][act], ref["lse"][act], label=f"step {s}")
