@@ -37,8 +37,11 @@ def lib():
         L.hso_merge.argtypes = [P, P, P, i32, i32, i32, P, P, P]
         L.hso_layer_transfer.argtypes = [P, P, i64, i64, i32, i32, i32, i32, i64, i64, P, P,
                                          i32, i64, i32, P]
+        L.hso_e4m3_decode.argtypes = [P, i64, P]
+        L.hso_fp8ds_dequant.argtypes = [P, i64, P, i64, P]
         for f in ("hso_normalize_indices", "hso_hot_lookup_assign", "hso_swap_in",
-                  "hso_backup", "hso_sparse_decode", "hso_merge", "hso_layer_transfer"):
+                  "hso_backup", "hso_sparse_decode", "hso_merge", "hso_layer_transfer",
+                  "hso_e4m3_decode", "hso_fp8ds_dequant"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -202,3 +205,48 @@ def merge(m, l, o):
     rc = lib().hso_merge(_p(m), _p(l), _p(o), n, parts, d_v, _p(mo), _p(lo), _p(oo))
     _check(rc, "hso_merge")
     return mo, lo, oo
+
+
+FP8DS_ROW_BYTES = 656
+
+
+def e4m3_decode(codes):
+    """OCP FP8 E4M3 codes (uint8 array) -> float64 values (NaN for 0x7F / 0xFF)."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _check(lib().hso_e4m3_decode(_p(codes), codes.size, _p(out)), "hso_e4m3_decode")
+    return out
+
+
+def fp8ds_dequant(rows8, ids=None):
+    """fp8_ds_mla rows (uint8 [n_rows, row_bytes >= 656]) -> bf16 bits uint16
+    [len(ids), 576]: latent column d = bf16(fp32(code) * fp32(scale[d // 128])),
+    RoPE columns copied.  ids: row numbers (default: every row)."""
+    rows8 = _c(rows8, np.uint8)
+    n_rows, row_bytes = rows8.shape
+    ids = np.arange(n_rows, dtype=np.int64) if ids is None else _c(ids, np.int64)
+    if ids.size and (ids.min() < 0 or ids.max() >= n_rows):
+        raise OracleError("fp8ds_dequant: row id out of range")
+    out = np.empty((ids.size, 576), np.uint16)
+    rc = lib().hso_fp8ds_dequant(_p(rows8), row_bytes, _p(ids), ids.size, _p(out))
+    _check(rc, "hso_fp8ds_dequant")
+    return out
+
+
+def sparse_decode_fp8ds(q, rows8, kv_rows, count, scale):
+    """S4 over fp8_ds_mla rows: every referenced row is reconstructed with
+    fp8ds_dequant, then sparse_decode runs on those bf16 rows (K = all 576
+    columns, V = the first 512).  Entries that are negative or beyond the
+    rows are masked (no row).  kv_rows int32 [rows, 1, cap]; count int32
+    [rows, 1] or None.  Returns (out float64 [rows, heads, 512], lse)."""
+    rows8 = _c(rows8, np.uint8)
+    kv_rows = _c(kv_rows, np.int32)
+    ok = (kv_rows >= 0) & (kv_rows < rows8.shape[0])
+    ids = np.unique(kv_rows[ok]).astype(np.int64)
+    deq = fp8ds_dequant(rows8, ids)
+    local = np.full(kv_rows.shape, -1, np.int32)
+    local[ok] = np.searchsorted(ids, kv_rows[ok]).astype(np.int32)
+    if deq.shape[0] == 0:
+        deq = np.zeros((1, 576), np.uint16)
+    flat = deq.reshape(-1)
+    return sparse_decode(q, flat, flat, 576, 0, local, count, scale, d_v=512)

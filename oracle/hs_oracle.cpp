@@ -425,4 +425,77 @@ int hso_merge(const double* m, const double* l, const double* o, int32_t n, int3
     return 0;
 }
 
+
+// ---------------------------------------------------------------------------
+// fp8_ds_mla KV rows ([HS] the FlashMLASparseBackend cache shape, the
+// FP8_DS_MLA_ROW_BYTES constant and the 656-byte copy walk-through of
+// Phase 5; [PT] 7.2 "量化 KV 与内核特化": the scale is applied to the stored
+// codes to reconstruct the values the attention computes with).
+//
+// One row is 656 bytes: bytes [0, 512) are the 512 latent (NoPE) columns as
+// OCP FP8 E4M3 codes, bytes [512, 528) are four IEEE binary32 scales
+// (little-endian), bytes [528, 656) are the 64 RoPE columns as bf16
+// (little-endian).  Readings: the 16 bytes of scales are four fp32 values and
+// scale g multiplies latent columns [128 g, 128 g + 128) (512 / 4); the value
+// of a latent column is code x scale, formed in binary32 (the scale's own
+// precision) and rounded to bf16, the operand precision of the attention
+// products (both roundings to nearest, ties to even).
+//
+// E4M3 from its definition: sign bit 7, exponent bits 6..3 (bias 7), mantissa
+// bits 2..0.  Exponent 0 is subnormal (m / 8 * 2^-6); exponent 15 with
+// mantissa 7 is NaN; there is no infinity (1111.110 = 448 is the largest).
+static double e4m3_to_double(uint8_t c) {
+    const int sgn = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+    if (e == 0)
+        v = std::ldexp(static_cast<double>(m) / 8.0, -6);
+    else
+        v = std::ldexp(1.0 + static_cast<double>(m) / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+// binary32 -> bf16 bits, round to nearest, ties to even (NaN stays a quiet NaN).
+static uint16_t float_to_bf16_rne(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof(u));
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return static_cast<uint16_t>((u >> 16) | 0x0040u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return static_cast<uint16_t>(u >> 16);
+}
+
+int hso_e4m3_decode(const uint8_t* codes, int64_t n, double* out) {
+    if (n < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
+    return 0;
+}
+
+// Rows ids[i] of `rows8` (row_bytes apart, row_bytes >= 656) -> out[i][576]
+// bf16 bits: latent columns reconstructed as above, RoPE columns copied.
+int hso_fp8ds_dequant(const uint8_t* rows8, int64_t row_bytes, const int64_t* ids, int64_t n,
+                      uint16_t* out) {
+    if (row_bytes < 656 || n < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint8_t* r = rows8 + ids[i] * row_bytes;
+        uint16_t* o = out + i * 576;
+        float scale[4];
+        for (int g = 0; g < 4; ++g) {
+            uint32_t u = 0;
+            for (int b = 0; b < 4; ++b) u |= static_cast<uint32_t>(r[512 + 4 * g + b]) << (8 * b);
+            std::memcpy(&scale[g], &u, sizeof(float));
+        }
+        for (int d = 0; d < 512; ++d) {
+            // The code's value is exact in binary32 (4 significant bits).
+            const float code = static_cast<float>(e4m3_to_double(r[d]));
+            const float v = code * scale[d / 128];
+            o[d] = float_to_bf16_rne(v);
+        }
+        for (int d = 0; d < 64; ++d)
+            o[512 + d] = static_cast<uint16_t>(r[528 + 2 * d] | (r[528 + 2 * d + 1] << 8));
+    }
+    return 0;
+}
+
 }  // extern "C"

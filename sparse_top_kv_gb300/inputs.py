@@ -23,6 +23,8 @@ Workloads (names used by the tests and the bench):
                   64 x 2048 pages), top_k 2048, hot 4096+1 rows per request;
                   step 0 uniform, later steps keep round(0.85*2048) = 1741 and
                   draw the rest Zipf(s=1.1) over recency rank r = T-1-t.
+  mla_decode_fp8  mla_decode with the paged cache stored as fp8_ds_mla rows of
+                  656 B (the same N(0,1) values, encoded by fp8ds_encode).
   gqa_union       16 requests, 32 query / 8 KV heads, d = 128, bshd caches of
                   65536 pages x 16 x 8 x 128 for K and V, random page table,
                   context 65536; one index row per (request, KV head): 922
@@ -226,6 +228,50 @@ def mla_decode(num_reqs=32, heads=128, top_k=2048, num_pages=16384, ctx=32768, d
         cfg["q"] = randn_bf16((num_reqs, heads, 576), seed + 200, device=device)
     cfg["cand"] = np.stack([rng.choice(ctx, size=top_k, replace=False)
                             for _ in range(num_reqs)]).astype(np.int32)
+    return cfg
+
+
+FP8DS_ROW_BYTES = 656
+
+
+def fp8ds_encode(values):
+    """Encode float rows [n, 576] as fp8_ds_mla rows, uint8 [n, 656]: columns
+    0..511 as E4M3 codes of value / scale (torch's float8_e4m3fn conversion),
+    with one fp32 scale per 128 columns = the group's largest magnitude / 448
+    (1 for an all-zero group) at bytes 512..527, and columns 512..575 as bf16
+    at bytes 528..655.  Input synthesis only: reading the rows back (the
+    dequantization the attention performs) is not done here."""
+    v = values.to(torch.float32)
+    n = v.shape[0]
+    lat = v[:, :512].reshape(n, 4, 128)
+    amax = lat.abs().amax(dim=2)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (lat / scale[:, :, None]).reshape(n, 512).to(torch.float8_e4m3fn)
+    out = torch.empty(n, FP8DS_ROW_BYTES, dtype=torch.uint8, device=v.device)
+    out[:, :512] = codes.view(torch.uint8)
+    out[:, 512:528] = scale.contiguous().view(torch.uint8).reshape(n, 16)
+    out[:, 528:] = v[:, 512:].to(torch.bfloat16).contiguous().view(torch.uint8).reshape(n, 128)
+    return out
+
+
+def mla_decode_fp8(device="cuda", with_data=True, **kw):
+    """Config mla_decode_fp8: mla_decode's indices, page table and query, with
+    the paged cache [num_pages * 64, 656] in fp8_ds_mla rows (encoded in
+    chunks on `device`)."""
+    cfg = mla_decode(device=device, with_data=False, **kw)
+    cfg["name"] = "mla_decode_fp8"
+    seed = SEEDS["mla_decode"]
+    if with_data:
+        n = cfg["num_pages"] * cfg["page_size"]
+        cache = torch.empty(n, FP8DS_ROW_BYTES, dtype=torch.uint8, device=device)
+        g = torch.Generator(device=device).manual_seed(seed + 100)
+        step = 1 << 17
+        for r0 in range(0, n, step):
+            r1 = min(n, r0 + step)
+            vals = torch.randn(r1 - r0, 576, generator=g, device=device, dtype=torch.float32)
+            cache[r0:r1] = fp8ds_encode(vals)
+        cfg["cache8"] = cache
+        cfg["q"] = randn_bf16((cfg["num_reqs"], cfg["heads"], 576), seed + 200, device=device)
     return cfg
 
 
