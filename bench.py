@@ -31,6 +31,7 @@ from sparse_top_kv_gb300.pipeline import HiSparseDecoder  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
 ROW_BYTES = 1152
+FP8DS_ROW_BYTES = 656
 # DRAM bytes (read + write) per launch from the ncu capture summarised in
 # profiles/step_kernels_full_hisparse.md (set to None when a kernel changes
 # after the capture).
@@ -512,6 +513,61 @@ def bench_mla_decode(hbm_peak, flush, reps=20):
             "s4_tflops": flops / t / 1e9, "workspace_bytes": ws}
 
 
+def bench_mla_decode_fp8(hbm_peak, flush, reps=20):
+    """mla_decode with the cache in fp8_ds_mla rows (656 B): S1, then
+    hs_sparse_decode_fp8ds (row reconstruction + tensor-core attention); the
+    reconstruction launch is also timed alone."""
+    cfg = inputs.mla_decode_fp8()
+    R, H = cfg["num_reqs"], cfg["heads"]
+    row_req = torch.arange(R, dtype=torch.int32, device="cuda")
+    seq = torch.full((R,), cfg["ctx"], dtype=torch.int32, device="cuda")
+    cand = torch.from_numpy(cfg["cand"]).cuda()
+    bt = torch.from_numpy(cfg["block_table"]).cuda()
+    out1 = hs.normalize_indices(cand, row_req, seq, bt, 64, num_pages=cfg["num_pages"])
+    tok, slot, count, err = out1
+    cap = slot.shape[1]
+    cache8 = cfg["cache8"]
+    out = torch.empty(R, H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(R, H, dtype=torch.float32, device="cuda")
+    ws = hs.sparse_decode_fp8ds_workspace_bytes(R, H, cap)
+    wsb = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(R * cap, 576, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(R * cap, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t_s4, t_g = [], []
+    for i in range(reps + 3):
+        flush_l2(flush)
+        host_headroom()
+        a, b, c = ev(), ev(), ev()
+        a.record()
+        hs.sparse_decode_fp8ds(cfg["q"], cache8, slot.view(R, 1, -1), count.view(R, 1),
+                               cfg["scale"], out=out, lse=lse, workspace=wsb, status=status)
+        b.record()
+        b.synchronize()
+        flush_l2(flush)
+        a2 = ev()
+        a2.record()
+        hs.fp8ds_gather(cache8, slot, count, out=scratch, out_ids=ids, status=status)
+        c.record()
+        c.synchronize()
+        if i >= 3:
+            t_s4.append(a.elapsed_time(b))
+            t_g.append(a2.elapsed_time(c))
+    assert status.item() == 0
+    n = R * 2048
+    nbytes = n * FP8DS_ROW_BYTES + R * H * 576 * 2 + R * H * 512 * 2 + n * 4 + R * H * 4
+    t = statistics.median(t_s4)
+    tg = statistics.median(t_g)
+    return {"workload": "mla_decode_fp8: 32 req x 128 heads, 2048 rows of 656 B fp8_ds_mla, "
+                        "paged HBM cache",
+            "s4_us": t * 1e3, "s4_bytes": nbytes, "s4_gbs": nbytes / t / 1e6,
+            "hbm_frac": nbytes / t / 1e6 / hbm_peak,
+            "reconstruct_us": tg * 1e3,
+            "reconstruct_gbs": n * (FP8DS_ROW_BYTES + ROW_BYTES) / tg / 1e6,
+            "design": "two launches: fp8 rows -> bf16 scratch (read 656 B, write 1152 B per row), "
+                      "then the tcgen05 MLA kernel over the scratch"}
+
+
 def bench_gqa(hbm_peak, flush, reps=20):
     cfg = inputs.gqa_union()
     R, G, d = cfg["num_reqs"], cfg["kv_heads"], cfg["d"]
@@ -760,6 +816,8 @@ def main():
     dominant = roof_attn if attn_ms >= swap_ms else roof_swap
     if world == 1 and not args.no_extras:
         extras["mla_decode"] = bench_mla_decode(hbm_peak, flush)
+        torch.cuda.empty_cache()
+        extras["mla_decode_fp8"] = bench_mla_decode_fp8(hbm_peak, flush)
         torch.cuda.empty_cache()
         extras["gqa_union"] = bench_gqa(hbm_peak, flush)
         torch.cuda.empty_cache()

@@ -370,6 +370,61 @@ int hs_sparse_decode_noalloc(const void* q, const void* k_base, const void* v_ba
 int hs_merge_states(const float* m, const float* l, const float* o, int32_t n, int32_t parts,
                     int32_t d_v, void* out, float* lse, hs_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * fp8_ds_mla rows -- [HS] the FlashMLASparseBackend cache shape and
+ * FP8_DS_MLA_ROW_BYTES = 656 (512 B quantised latent + 16 B scales + 128 B
+ * RoPE), the 656-byte row of the Phase 5 copy walk-through; [PT] 7.2
+ * (quantised KV: the scale is applied to the stored codes before the
+ * products).  One row, 656 bytes (rows may sit row_bytes >= 656 apart):
+ *   bytes [0, 512)    latent columns 0..511 as OCP FP8 E4M3 codes;
+ *   bytes [512, 528)  four fp32 scales; scale g covers latent columns
+ *                     [128 g, 128 g + 128);
+ *   bytes [528, 656)  RoPE columns 512..575 as bf16.
+ * Value of latent column d: code_d * scale_{d/128} in fp32, rounded to bf16
+ * (nearest, ties to even) -- the operand type of QK^T and PV.  The hot
+ * buffer, SwapIn and BackUp move these rows as opaque 656-byte rows
+ * (row_bytes = 656 is a multiple of 16).
+ *
+ * hs_fp8ds_gather -- reconstruct the selected rows into a bf16 scratch.
+ * kv8        device (or mapped pinned) rows, 16-byte aligned, row_bytes apart
+ *            (multiple of 16, >= 656), num_kv_rows rows.
+ * kv_rows    int32 [rows, cap] row ids; entries j >= count[r] are ignored;
+ *            a negative id is no row (-1 is padding); an id >= num_kv_rows
+ *            is no row and sets HS_ERR_BAD_INDEX in *status.
+ * count      int32 [rows] or NULL (= cap).
+ * out        bf16 [rows * cap, 576], 16-byte aligned: row r * cap + j holds
+ *            the reconstructed row of kv_rows[r][j] (rows with no row id and
+ *            rows j >= count[r] are not written).
+ * out_ids    int32 [rows * cap]: r * cap + j where a row was written, -1
+ *            where kv_rows[r][j] is no row (j >= count[r] not written): the
+ *            kv_rows of a hs_sparse_decode over `out`.
+ * Returns HS_ERR_INVALID_ARG (negative sizes, null pointers, row_bytes <
+ * 656), HS_ERR_MISALIGNED, HS_ERR_CAPACITY (rows * cap >= 2^31).
+ *
+ * hs_sparse_decode_fp8ds -- S4 (MLA shape: K = all 576 columns, V = the
+ * first 512, kv_heads = 1) over fp8_ds_mla rows: hs_fp8ds_gather into the
+ * workspace, then hs_sparse_decode over the reconstructed rows.  q, out, lse,
+ * count, scale, status as for hs_sparse_decode; kv_rows int32 [rows, cap].
+ * workspace  device, 256-byte aligned, at least
+ *            hs_sparse_decode_fp8ds_workspace_bytes(rows, heads, cap) bytes
+ *            (the bf16 scratch rows * cap * 1152 B, the ids, and
+ *            hs_sparse_decode's own workspace); caller-owned, no contents
+ *            need to survive between calls.
+ * Returns the first failing status of the two launches (HS_ERR_CAPACITY
+ * when the workspace is missing or too small).
+ * ------------------------------------------------------------------------- */
+int hs_fp8ds_gather(const void* kv8, int64_t row_bytes, int64_t num_kv_rows,
+                    const int32_t* kv_rows, const int32_t* count, int32_t rows, int32_t cap,
+                    void* out, int32_t* out_ids, int32_t* status, hs_stream_t stream);
+
+int64_t hs_sparse_decode_fp8ds_workspace_bytes(int32_t rows, int32_t heads, int32_t cap);
+
+int hs_sparse_decode_fp8ds(const void* q, const void* kv8, int64_t row_bytes,
+                           int64_t num_kv_rows, const int32_t* kv_rows, const int32_t* count,
+                           int32_t rows, int32_t cap, int32_t heads, float scale, void* out,
+                           float* lse, void* workspace, int64_t workspace_bytes_given,
+                           int32_t* status, hs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

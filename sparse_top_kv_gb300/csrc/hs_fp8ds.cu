@@ -1,0 +1,203 @@
+// hs_fp8ds.cu -- S4 over fp8_ds_mla KV rows.
+//
+// Row format (vLLM HiSparse walkthrough: the FlashMLASparseBackend cache shape
+// and FP8_DS_MLA_ROW_BYTES = 656): bytes [0, 512) hold the 512 latent
+// columns as OCP FP8 E4M3 codes, bytes [512, 528) four fp32 scales (scale g
+// for latent columns [128 g, 128 g + 128)), bytes [528, 656) the 64 RoPE
+// columns as bf16.  Column d < 512 has the value code_d * scale_{d/128},
+// formed in fp32 and rounded to bf16, the operand type of the products
+// (PaperTrace 5.1.1 section 7.2: the scale is applied to the stored codes
+// before QK^T and PV).
+//
+// GB300 design.  The attention runs in two launches:
+//  * fp8ds_gather_kernel: one warp per selected row; lane i loads the codes
+//    of columns 8 i .. 8 i + 7 and 256 + 8 i .. 263 + 8 i (two 8-byte
+//    loads), their group scales, lanes 0-7 the RoPE bytes; the codes go
+//    through the hardware e4m3x2 -> f16x2 conversion, fp32 scaling and bf16
+//    rounding, and the warp writes the 1152-byte bf16 row into a per-request
+//    scratch [rows, cap, 576] with fully coalesced stores.  Each warp keeps
+//    four rows in flight.
+//  * the tcgen05 MLA kernel (hs_attention_mla.cu) attends over the scratch
+//    rows of each request (row ids r * cap + j).
+// The reconstructed rows cross HBM/L2 once more than a dequantising load
+// path would; the scratch of one decode batch (72 MB for 32 x 2048 rows) is
+// written just before the attention reads it, and mostly stays in L2.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "hs_common.cuh"
+
+namespace {
+
+constexpr int kFp8RowBytes = 656;
+constexpr int kRowsPerWarp = 4;
+constexpr int kThreads = 256;
+
+struct GatherArgs {
+    const unsigned char* kv8;
+    int64_t row_bytes;
+    int64_t num_kv_rows;
+    const int32_t* kv_rows;  // [rows, cap]
+    const int32_t* count;    // [rows] or null (= cap)
+    int32_t rows;
+    int32_t cap;
+    __nv_bfloat16* out;      // [rows * cap, 576]
+    int32_t* out_ids;        // [rows * cap]: r * cap + j, or -1 (no row)
+    int32_t* status;
+};
+
+// Eight E4M3 codes (one 8-byte word) -> eight bf16 values code * scale.
+__device__ __forceinline__ uint4 dequant8(uint2 codes, float scale) {
+    uint32_t w[2] = {codes.x, codes.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t word = w[k >> 1];
+        const __nv_fp8x2_storage_t pair =
+            static_cast<__nv_fp8x2_storage_t>((k & 1) ? (word >> 16) : (word & 0xFFFFu));
+        const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
+        const float2 f = __half22float2(h);
+        const __nv_bfloat162 b =
+            __floats2bfloat162_rn(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
+        o[k] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Lane i of a warp owns latent columns [8 i, 8 i + 8) and [256 + 8 i, 264 + 8 i)
+// (scale groups i / 16 and 2 + i / 16): each of its two 8-byte code loads and
+// each of its two 16-byte stores is one fully coalesced 256-byte / 512-byte
+// warp access.  Lanes 0-7 also move the 128 RoPE bytes.
+__global__ void __launch_bounds__(kThreads) fp8ds_gather_kernel(const GatherArgs a) {
+    hs::pdl_trigger();
+    hs::pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+    const int64_t total = int64_t(a.rows) * a.cap;
+    bool bad = false;
+    for (int64_t base = warp0 * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
+        uint2 lo[kRowsPerWarp], hi[kRowsPerWarp];
+        uint4 rope[kRowsPerWarp];
+        float s_lo[kRowsPerWarp], s_hi[kRowsPerWarp];
+        int32_t id[kRowsPerWarp];
+        bool live[kRowsPerWarp];
+        // All loads of the warp's rows first.
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp; ++u) {
+            const int64_t f = base + u;
+            live[u] = false;
+            id[u] = -1;
+            if (f < total) {
+                const int r = int(f / a.cap), j = int(f - int64_t(r) * a.cap);
+                const int n = a.count ? min(max(__ldg(a.count + r), 0), a.cap) : a.cap;
+                if (j < n) {
+                    live[u] = true;
+                    id[u] = __ldg(a.kv_rows + f);
+                }
+            }
+            const bool v = live[u] && id[u] >= 0 && int64_t(id[u]) < a.num_kv_rows;
+            if (live[u] && int64_t(id[u]) >= a.num_kv_rows) bad = true;
+            if (!v) id[u] = -1;
+            if (id[u] >= 0) {
+                const unsigned char* row = a.kv8 + int64_t(id[u]) * a.row_bytes;
+                lo[u] = __ldg(reinterpret_cast<const uint2*>(row) + lane);
+                hi[u] = __ldg(reinterpret_cast<const uint2*>(row + 256) + lane);
+                const float* sc = reinterpret_cast<const float*>(row + 512);
+                s_lo[u] = __ldg(sc + (lane >> 4));
+                s_hi[u] = __ldg(sc + 2 + (lane >> 4));
+                if (lane < 8) rope[u] = __ldg(reinterpret_cast<const uint4*>(row + 528) + lane);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp; ++u) {
+            const int64_t f = base + u;
+            if (!live[u]) continue;
+            if (lane == 0) a.out_ids[f] = id[u] >= 0 ? int32_t(f) : -1;
+            if (id[u] < 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + f * 576);
+            dst[lane] = dequant8(lo[u], s_lo[u]);
+            dst[32 + lane] = dequant8(hi[u], s_hi[u]);
+            if (lane < 8) dst[64 + lane] = rope[u];
+        }
+    }
+    if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+}
+
+int gather_ctas_per_sm() {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fp8ds_gather_kernel, kThreads, 0) !=
+                cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            n = 1;
+        }
+        per_sm = n;
+    }
+    return per_sm;
+}
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+}  // namespace
+
+extern "C" int hs_fp8ds_gather(const void* kv8, int64_t row_bytes, int64_t num_kv_rows,
+                               const int32_t* kv_rows, const int32_t* count, int32_t rows,
+                               int32_t cap, void* out, int32_t* out_ids, int32_t* status,
+                               hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || num_kv_rows < 0 || row_bytes < kFp8RowBytes)
+        return HS_ERR_INVALID_ARG;
+    if (row_bytes % 16) return HS_ERR_MISALIGNED;
+    const int64_t total = int64_t(rows) * cap;
+    if (total == 0) return HS_OK;
+    if (total > INT32_MAX) return HS_ERR_CAPACITY;
+    if (kv8 == nullptr || kv_rows == nullptr || out == nullptr || out_ids == nullptr)
+        return HS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kv8) | reinterpret_cast<uintptr_t>(out)) & 15u)
+        return HS_ERR_MISALIGNED;
+    const GatherArgs a{static_cast<const unsigned char*>(kv8), row_bytes, num_kv_rows, kv_rows,
+                       count, rows, cap, static_cast<__nv_bfloat16*>(out), out_ids, status};
+    const int64_t warps = (total + kRowsPerWarp - 1) / kRowsPerWarp;
+    const int64_t ctas = hs::min64((warps * 32 + kThreads - 1) / kThreads,
+                                   int64_t(hs_host::num_sms()) * gather_ctas_per_sm());
+    return hs_host::launch_pdl(fp8ds_gather_kernel, dim3(unsigned(ctas)), dim3(kThreads), 0,
+                               stream, a);
+}
+
+extern "C" int64_t hs_sparse_decode_fp8ds_workspace_bytes(int32_t rows, int32_t heads,
+                                                          int32_t cap) {
+    if (rows < 0 || heads <= 0 || cap < 0) return -1;
+    const int64_t total = int64_t(rows) * cap;
+    const int64_t dec = hs_sparse_decode_workspace_bytes(rows, heads, 1, cap, 576, 512);
+    if (dec < 0) return -1;
+    return align256(total * 576 * 2) + align256(total * 4) + dec;
+}
+
+extern "C" int hs_sparse_decode_fp8ds(const void* q, const void* kv8, int64_t row_bytes,
+                                      int64_t num_kv_rows, const int32_t* kv_rows,
+                                      const int32_t* count, int32_t rows, int32_t cap,
+                                      int32_t heads, float scale, void* out, float* lse,
+                                      void* workspace, int64_t workspace_bytes_given,
+                                      int32_t* status, hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || heads <= 0) return HS_ERR_INVALID_ARG;
+    if (rows == 0) return HS_OK;
+    const int64_t need = hs_sparse_decode_fp8ds_workspace_bytes(rows, heads, cap);
+    if (need < 0) return HS_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes_given < need) return HS_ERR_CAPACITY;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return HS_ERR_MISALIGNED;
+    const int64_t total = int64_t(rows) * cap;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    void* scratch = ws;
+    int32_t* ids = reinterpret_cast<int32_t*>(ws + align256(total * 576 * 2));
+    unsigned char* dec_ws = ws + align256(total * 576 * 2) + align256(total * 4);
+    const int64_t dec_bytes = need - (dec_ws - ws);
+    int rc = hs_fp8ds_gather(kv8, row_bytes, num_kv_rows, kv_rows, count, rows, cap, scratch,
+                             ids, status, stream);
+    if (rc != HS_OK) return rc;
+    return hs_sparse_decode(q, scratch, scratch, 576, 0, total, ids, count, rows, cap, heads, 1,
+                            576, 512, scale, out, lse, dec_bytes > 0 ? dec_ws : nullptr,
+                            dec_bytes, status, stream);
+}

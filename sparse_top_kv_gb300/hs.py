@@ -56,6 +56,10 @@ _SIGS = {
                                 ctypes.c_int),
     "hs_sparse_decode_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32,
                                   _I32, _I32, _F32, _P, _P, _P, _P], ctypes.c_int),
+    "hs_fp8ds_gather": ([_P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
+    "hs_sparse_decode_fp8ds_workspace_bytes": ([_I32, _I32, _I32], _I64),
+    "hs_sparse_decode_fp8ds": ([_P, _P, _I64, _I64, _P, _P, _I32, _I32, _I32, _F32, _P, _P, _P,
+                                _I64, _P, _P], ctypes.c_int),
 }
 
 NOALLOC_WORKSPACE_BYTES = 8 * 1024 * 1024  # HS_NOALLOC_WORKSPACE_BYTES
@@ -284,6 +288,58 @@ def sparse_decode(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv
           num_kv_rows, _ptr(kv_rows), _ptr(count), rows, cap, heads, kv_heads, d_qk, d_v,
           float(scale), _ptr(out), _ptr(lse), _ptr(workspace) if ws > 0 else None,
           workspace.numel() * workspace.element_size() if (ws > 0) else 0, _ptr(status),
+          _stream(stream))
+    return out, lse
+
+
+FP8DS_ROW_BYTES = 656
+
+
+def fp8ds_gather(kv8, kv_rows, count, *, out=None, out_ids=None, status=None, stream=None):
+    """Reconstruct fp8_ds_mla rows.  kv8 uint8 [num_kv_rows, row_bytes >= 656];
+    kv_rows int32 [rows, cap]; count int32 [rows] or None.  Returns (out bf16
+    [rows * cap, 576], out_ids int32 [rows * cap])."""
+    _check(kv8, torch.uint8, "kv8")
+    _check(kv_rows, torch.int32, "kv_rows")
+    _check(count, torch.int32, "count")
+    _check(status, torch.int32, "status")
+    rows, cap = kv_rows.shape[0], kv_rows.shape[-1]
+    if out is None:
+        out = torch.empty(rows * cap, 576, dtype=torch.bfloat16, device=kv_rows.device)
+    if out_ids is None:
+        out_ids = torch.empty(rows * cap, dtype=torch.int32, device=kv_rows.device)
+    _call("hs_fp8ds_gather", _ptr(kv8), kv8.shape[1], kv8.shape[0], _ptr(kv_rows), _ptr(count),
+          rows, cap, _ptr(out), _ptr(out_ids), _ptr(status), _stream(stream))
+    return out, out_ids
+
+
+def sparse_decode_fp8ds_workspace_bytes(rows, heads, cap):
+    return int(lib().hs_sparse_decode_fp8ds_workspace_bytes(rows, heads, cap))
+
+
+def sparse_decode_fp8ds(q, kv8, kv_rows, count, scale, *, out=None, lse=None, workspace=None,
+                        status=None, stream=None):
+    """S4 over fp8_ds_mla rows (MLA shape).  q bf16 [rows, heads, 576]; kv8
+    uint8 [num_kv_rows, row_bytes >= 656]; kv_rows int32 [rows, 1, cap] or
+    [rows, cap]; count int32 [rows] / [rows, 1] or None.  Returns (out bf16
+    [rows, heads, 512], lse fp32 [rows, heads])."""
+    _check(q, torch.bfloat16, "q")
+    _check(kv8, torch.uint8, "kv8")
+    _check(kv_rows, torch.int32, "kv_rows")
+    _check(count, torch.int32, "count")
+    _check(status, torch.int32, "status")
+    rows, heads, _ = q.shape
+    cap = kv_rows.shape[-1]
+    if out is None:
+        out = torch.empty(rows, heads, 512, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=q.device)
+    ws = sparse_decode_fp8ds_workspace_bytes(rows, heads, cap)
+    if workspace is None or workspace.numel() * workspace.element_size() < ws:
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    _call("hs_sparse_decode_fp8ds", _ptr(q), _ptr(kv8), kv8.shape[1], kv8.shape[0],
+          _ptr(kv_rows), _ptr(count), rows, cap, heads, float(scale), _ptr(out), _ptr(lse),
+          _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
           _stream(stream))
     return out, lse
 

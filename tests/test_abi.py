@@ -64,6 +64,13 @@ def test_host_side_argument_checks():
     assert L.hs_layer_transfer(P, P, 60, 0, 1, 1, 16, 1, 64, 96, P, P, 4, 1, 0, 0, P, P) == 1
     assert L.hs_layer_transfer(P, P, 64, 0, 1, 1, 16, 0, 64, 16384, P, P, 4, 1, 0, 0, P,
                                P) == 3
+    # fp8_ds_mla rows: rows shorter than 656 B, a stride that is not a
+    # multiple of 16, a missing workspace, negative sizes.
+    assert L.hs_fp8ds_gather(P, 640, 10, P, P, 1, 4, P, P, P, P) == 1
+    assert L.hs_fp8ds_gather(P, 664, 10, P, P, 1, 4, P, P, P, P) == 2
+    assert L.hs_fp8ds_gather(P, 656, 10, P, P, 0, 4, P, P, P, P) == 0
+    assert L.hs_sparse_decode_fp8ds_workspace_bytes(-1, 16, 64) == -1
+    assert L.hs_sparse_decode_fp8ds(P, P, 656, 10, P, P, 1, 64, 16, 1.0, P, P, P, 0, P, P) == 3
     # Unsupported attention shape, null pointers.
     buf = ctypes.create_string_buffer(4096)
     p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 16), ctypes.c_void_p)
