@@ -17,16 +17,19 @@
 //    rounding, and the warp writes the 1152-byte bf16 row into a per-request
 //    scratch [rows, cap, 576] with fully coalesced stores.  Each warp keeps
 //    four rows in flight.
-//  * the tcgen05 MLA kernel (hs_attention_mla.cu) attends over the scratch
-//    rows of each request (row ids r * cap + j).
-// The reconstructed rows cross HBM/L2 once more than a dequantising load
-// path would; the scratch of one decode batch (72 MB for 32 x 2048 rows) is
-// written just before the attention reads it, and mostly stays in L2.
+//  * the MLA attention (hs_attention_mla.cu on tensor cores for head counts
+//    that are multiples of 16) over the scratch rows of each request (row
+//    ids r * cap + j).
+// The reconstructed rows cross HBM/L2 once more than a reconstructing load
+// path would (PaperTrace section 7.2 prefers the latter).  Reconstructing in
+// the tensor-core kernel's loaders was built and measured slower on GB300:
+// the code -> fp32 * scale -> bf16 conversion of a whole 128-row unit lies
+// between its arrival and the MMA, and the few warps that can do it bound
+// the per-tile time.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "hs_common.cuh"
+#include "hs_fp8.cuh"
 
 namespace {
 
@@ -46,24 +49,6 @@ struct GatherArgs {
     int32_t* out_ids;        // [rows * cap]: r * cap + j, or -1 (no row)
     int32_t* status;
 };
-
-// Eight E4M3 codes (one 8-byte word) -> eight bf16 values code * scale.
-__device__ __forceinline__ uint4 dequant8(uint2 codes, float scale) {
-    uint32_t w[2] = {codes.x, codes.y};
-    uint32_t o[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t word = w[k >> 1];
-        const __nv_fp8x2_storage_t pair =
-            static_cast<__nv_fp8x2_storage_t>((k & 1) ? (word >> 16) : (word & 0xFFFFu));
-        const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
-        const float2 f = __half22float2(h);
-        const __nv_bfloat162 b =
-            __floats2bfloat162_rn(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
-        o[k] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
 
 // Lane i of a warp owns latent columns [8 i, 8 i + 8) and [256 + 8 i, 264 + 8 i)
 // (scale groups i / 16 and 2 + i / 16): each of its two 8-byte code loads and
@@ -117,8 +102,8 @@ __global__ void __launch_bounds__(kThreads) fp8ds_gather_kernel(const GatherArgs
             if (lane == 0) a.out_ids[f] = id[u] >= 0 ? int32_t(f) : -1;
             if (id[u] < 0) continue;
             uint4* dst = reinterpret_cast<uint4*>(a.out + f * 576);
-            dst[lane] = dequant8(lo[u], s_lo[u]);
-            dst[32 + lane] = dequant8(hi[u], s_hi[u]);
+            dst[lane] = hs::fp8_dequant8(lo[u], s_lo[u]);
+            dst[32 + lane] = hs::fp8_dequant8(hi[u], s_hi[u]);
             if (lane < 8) dst[64 + lane] = rope[u];
         }
     }

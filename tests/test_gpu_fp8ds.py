@@ -110,10 +110,10 @@ def decode_fp8_both(q, rows8_np, rows8_dev, kv_rows, count, scale, sample_rows=N
     return int(status.item())
 
 
-@pytest.mark.parametrize("heads", [16, 64, 128])
+@pytest.mark.parametrize("heads", [16, 20, 64, 128])
 def test_decode_small(heads):
     """Lists of up to 600 rows (several 128-row tiles, ragged tails), holes,
-    one empty list."""
+    one empty list; 20 heads attend on the CUDA-core MLA kernel."""
     rng = np.random.default_rng(20 + heads)
     rows, n_kv, cap = 3, 2000, 600
     vals = torch.from_numpy(rng.standard_normal((n_kv, 576)).astype(np.float32))
@@ -126,6 +126,21 @@ def test_decode_small(heads):
         count[r, 0] = n
     kv_rows[0, 0, [5, 77]] = -1
     assert decode_fp8_both(q, rows8, cuda(rows8), kv_rows, count, 1 / 24) == 0
+
+
+@pytest.mark.parametrize("rows,heads,cap", [(152, 16, 384), (76, 128, 256), (40, 32, 1000)])
+def test_decode_many_tiles_per_cta(rows, heads, cap):
+    """Enough rows that each attention CTA walks several 128-row tiles of the
+    reconstructed rows."""
+    rng = np.random.default_rng(rows + heads)
+    n_kv = 20000
+    vals = torch.from_numpy(rng.standard_normal((n_kv, 576)).astype(np.float32))
+    rows8 = inputs.fp8ds_encode(vals).numpy()
+    q = inputs.randn_bf16((rows, heads, 576), 44, device="cuda")
+    kv_rows = np.stack([rng.choice(n_kv, cap, replace=False) for _ in range(rows)])
+    count = np.maximum(rng.integers(1, cap + 1, rows), cap - 5).astype(np.int32)
+    assert decode_fp8_both(q, rows8, cuda(rows8), kv_rows[:, None].astype(np.int32),
+                           count[:, None], 1 / 24, sample_rows=[0, 1, rows // 2, rows - 1]) == 0
 
 
 def test_decode_tail_sizes_and_bad_ids():
