@@ -136,8 +136,8 @@ def ev():
 
 
 # ----------------------------------------------------------------------------
-def setup_full(steps, rank):
-    cfg = inputs.full_hisparse(steps=steps)
+def setup_full(steps, rank, row_format="bf16"):
+    cfg = inputs.full_hisparse(steps=steps, row_format=row_format)
     # Weak scaling: every rank serves its own batch of requests.
     cfg["block_table"] = cfg["block_table"][replicas.rank_request_order(cfg["num_reqs"], rank)]
     return cfg
@@ -148,7 +148,7 @@ def make_decoder(cfg):
                            num_pages=cfg["num_pages"], page_size=cfg["page_size"],
                            top_k=cfg["top_k"], hot_size=cfg["hot_size"],
                            region_stride=cfg["region_stride"], heads=cfg["heads"],
-                           scale=cfg["scale"])
+                           scale=cfg["scale"], row_format=cfg.get("row_format", "bf16"))
 
 
 def device_inputs(cfg, dec):
@@ -179,7 +179,7 @@ def warm_host_memory(cfg, steps):
     torch.cuda.empty_cache()
 
 
-def run_full(args, rank, world, flush):
+def run_full(args, rank, world, flush, row_format="bf16"):
     """Step 0 (the all-miss cold step) runs eagerly, which also performs the
     library's one-time set-up; the step is then captured as a CUDA graph once
     per step's input slot (each step's packed inputs are resident in HBM in
@@ -190,7 +190,7 @@ def run_full(args, rank, world, flush):
     after the decoder state (hot buffer, dgi, lru, stats) is restored to its
     value before the timed steps; those events are not in the timed steps."""
     S = args.warmup + args.steps
-    cfg = setup_full(S, rank)
+    cfg = setup_full(S, rank, row_format)
     warm_host_memory(cfg, S)
     dec = make_decoder(cfg)
     dec.warm_pool()
@@ -266,7 +266,7 @@ def run_full(args, rank, world, flush):
         dec.graph = g_plain
         assert int(dec.status.item()) == 0, f"device status {dec.status.item()}"
     del snapshot
-    swap_bytes = miss_total * ROW_BYTES
+    swap_bytes = miss_total * dec.row_bytes
     total_ms = replicas.max_over_ranks(total_ms)
     K = args.steps
     res = dict(total_ms=total_ms, K=K, stage_ms=(stage_ms / K).tolist(),
@@ -568,6 +568,25 @@ def bench_mla_decode_fp8(hbm_peak, flush, reps=20):
                       "then the tcgen05 MLA kernel over the scratch"}
 
 
+def bench_full_fp8(args, flush):
+    """full_hisparse with the pool and the new rows as fp8_ds_mla rows (656 B):
+    the same index streams, decoder and timed graph replays as the headline;
+    SwapIn moves 656 bytes per miss and reconstructs bf16 hot rows."""
+    r = run_full(args, 0, 1, flush, row_format="fp8ds")
+    K = r["K"]
+    st = r["stage_ms"]
+    out = {"workload": "full_hisparse_fp8: full_hisparse with fp8_ds_mla rows (pinned pool "
+                       "5.50 GB, 656 B per row), bf16 hot buffer",
+           "steps_per_s": K / (r["total_ms"] / 1e3), "ms_per_step": r["total_ms"] / K,
+           "hit_rate": r["hit_rate"], "swap_bytes_per_step": r["swap_bytes_per_step"],
+           "stage_us": {"s1": st[0] * 1e3, "s2": st[1] * 1e3, "swap_in": st[3] * 1e3,
+                        "resident_rows": st[4] * 1e3, "swapped_rows_merge": st[5] * 1e3},
+           "swap_in_gbs": r["swap_bytes_per_step"] / (st[3] * 1e6) if st[3] > 0 else None,
+           "clocks": r["clocks"]}
+    del r
+    return out
+
+
 def bench_gqa(hbm_peak, flush, reps=20):
     cfg = inputs.gqa_union()
     R, G, d = cfg["num_reqs"], cfg["kv_heads"], cfg["d"]
@@ -822,6 +841,8 @@ def main():
         extras["gqa_union"] = bench_gqa(hbm_peak, flush)
         torch.cuda.empty_cache()
         extras["hicache"] = bench_hicache()
+        torch.cuda.empty_cache()
+        extras["full_hisparse_fp8"] = bench_full_fp8(args, flush)
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

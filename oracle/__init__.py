@@ -39,9 +39,10 @@ def lib():
                                          i32, i64, i32, P]
         L.hso_e4m3_decode.argtypes = [P, i64, P]
         L.hso_fp8ds_dequant.argtypes = [P, i64, P, i64, P]
+        L.hso_swap_in_fp8ds.argtypes = [P, i64, i64, P, P, P, P, i32, i32, P, i32, i64]
         for f in ("hso_normalize_indices", "hso_hot_lookup_assign", "hso_swap_in",
                   "hso_backup", "hso_sparse_decode", "hso_merge", "hso_layer_transfer",
-                  "hso_e4m3_decode", "hso_fp8ds_dequant"):
+                  "hso_e4m3_decode", "hso_fp8ds_dequant", "hso_swap_in_fp8ds"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -250,3 +251,20 @@ def sparse_decode_fp8ds(q, rows8, kv_rows, count, scale):
         deq = np.zeros((1, 576), np.uint16)
     flat = deq.reshape(-1)
     return sparse_decode(q, flat, flat, 576, 0, local, count, scale, d_v=512)
+
+
+def swap_in_fp8ds(host_pool8, hot, miss_src, miss_dst, miss_count, dgi=None, hot_size=0,
+                  region_stride=0):
+    """S3 SwapIn from fp8_ds_mla pool rows (uint8 [host_rows, row_bytes >= 656])
+    into bf16 hot rows (uint16 bits [hot_rows, 576], updated in place), each
+    copied row reconstructed as in fp8ds_dequant."""
+    host_pool8 = _c(host_pool8, np.uint8)
+    miss_src = _c(miss_src, np.int32)
+    miss_dst = _c(miss_dst, np.int64)
+    miss_count = _c(miss_count, np.int32)
+    assert hot.dtype == np.uint16 and hot.flags.c_contiguous and hot.shape[-1] == 576
+    rows, cap = miss_src.shape
+    rc = lib().hso_swap_in_fp8ds(_p(host_pool8), host_pool8.shape[0], host_pool8.shape[1],
+                                 _p(hot), _p(miss_src), _p(miss_dst), _p(miss_count), rows, cap,
+                                 _p(dgi), hot_size, region_stride)
+    _check(rc, "hso_swap_in_fp8ds")

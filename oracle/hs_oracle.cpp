@@ -472,28 +472,57 @@ int hso_e4m3_decode(const uint8_t* codes, int64_t n, double* out) {
     return 0;
 }
 
-// Rows ids[i] of `rows8` (row_bytes apart, row_bytes >= 656) -> out[i][576]
-// bf16 bits: latent columns reconstructed as above, RoPE columns copied.
+// One 656-byte row -> 576 bf16 bits: latent columns reconstructed as above,
+// RoPE columns copied.
+static void fp8ds_row(const uint8_t* r, uint16_t* o) {
+    float scale[4];
+    for (int g = 0; g < 4; ++g) {
+        uint32_t u = 0;
+        for (int b = 0; b < 4; ++b) u |= static_cast<uint32_t>(r[512 + 4 * g + b]) << (8 * b);
+        std::memcpy(&scale[g], &u, sizeof(float));
+    }
+    for (int d = 0; d < 512; ++d) {
+        // The code's value is exact in binary32 (4 significant bits).
+        const float code = static_cast<float>(e4m3_to_double(r[d]));
+        const float v = code * scale[d / 128];
+        o[d] = float_to_bf16_rne(v);
+    }
+    for (int d = 0; d < 64; ++d)
+        o[512 + d] = static_cast<uint16_t>(r[528 + 2 * d] | (r[528 + 2 * d + 1] << 8));
+}
+
+// Rows ids[i] of `rows8` (row_bytes apart, row_bytes >= 656) -> out[i][576].
 int hso_fp8ds_dequant(const uint8_t* rows8, int64_t row_bytes, const int64_t* ids, int64_t n,
                       uint16_t* out) {
     if (row_bytes < 656 || n < 0) return 1;
-    for (int64_t i = 0; i < n; ++i) {
-        const uint8_t* r = rows8 + ids[i] * row_bytes;
-        uint16_t* o = out + i * 576;
-        float scale[4];
-        for (int g = 0; g < 4; ++g) {
-            uint32_t u = 0;
-            for (int b = 0; b < 4; ++b) u |= static_cast<uint32_t>(r[512 + 4 * g + b]) << (8 * b);
-            std::memcpy(&scale[g], &u, sizeof(float));
+    for (int64_t i = 0; i < n; ++i) fp8ds_row(rows8 + ids[i] * row_bytes, out + i * 576);
+    return 0;
+}
+
+// SwapIn from a pool of fp8_ds_mla rows into a hot buffer of bf16 rows
+// (576 columns): the hso_swap_in walk, with each copied row reconstructed by
+// fp8ds_row.  A source outside the pool zeroes the hot row and revokes its
+// slot, as in hso_swap_in.
+int hso_swap_in_fp8ds(const uint8_t* host_pool8, int64_t host_rows, int64_t host_row_bytes,
+                      uint16_t* hot, const int32_t* miss_src, const int64_t* miss_dst,
+                      const int32_t* miss_count, int32_t rows, int32_t cap, int32_t* dgi,
+                      int32_t hot_size, int64_t region_stride) {
+    if (host_row_bytes < 656) return 1;
+    for (int32_t r = 0; r < rows; ++r) {
+        for (int32_t m = 0; m < miss_count[r]; ++m) {
+            const int64_t g = miss_src[static_cast<int64_t>(r) * cap + m];
+            const int64_t dst = miss_dst[static_cast<int64_t>(r) * cap + m];
+            uint16_t* to = hot + dst * 576;
+            if (g >= 0 && g < host_rows) {
+                fp8ds_row(host_pool8 + g * host_row_bytes, to);
+            } else {
+                for (int d = 0; d < 576; ++d) to[d] = 0;
+                if (dgi != nullptr) {
+                    const int64_t s = dst - static_cast<int64_t>(r) * region_stride;
+                    if (s >= 0 && s < hot_size) dgi[static_cast<int64_t>(r) * hot_size + s] = -1;
+                }
+            }
         }
-        for (int d = 0; d < 512; ++d) {
-            // The code's value is exact in binary32 (4 significant bits).
-            const float code = static_cast<float>(e4m3_to_double(r[d]));
-            const float v = code * scale[d / 128];
-            o[d] = float_to_bf16_rne(v);
-        }
-        for (int d = 0; d < 64; ++d)
-            o[512 + d] = static_cast<uint16_t>(r[528 + 2 * d] | (r[528 + 2 * d + 1] << 8));
     }
     return 0;
 }

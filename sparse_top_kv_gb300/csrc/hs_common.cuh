@@ -172,7 +172,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
 
 // ----------------------------------------------------------------------------
 // Programmatic dependent launch (PTX griddepcontrol).  Every kernel of the
-// library lets its dependents start launching at once (pdl_trigger), and
+// library lets its dependents start launching (pdl_trigger) at once, except
+// the fp8 row reconstruction, which does so when it is done, and
 // the kernels on the decode step's critical path are launched with
 // programmatic stream serialization, so each may start while its stream
 // predecessor still runs.  Rule kept by every such kernel: before pdl_wait

@@ -58,6 +58,8 @@ struct XferArgs {
     int32_t* dgi;           // swap-in revocation target, or nullptr
     int32_t zero_bad_src;   // 1: a missing source zeroes the destination (SwapIn)
     int32_t pad_dst;        // 1: a destination id of -1 is padding, skipped silently (BackUp)
+    int32_t dst_by_entry;   // 1: entry m of list r goes to row r * list_stride + m (staging)
+    int32_t skip_bad_src;   // 1: an entry without a source row is skipped silently
     int32_t hot_size;
     int64_t region_stride;
     int32_t* status;
@@ -190,7 +192,8 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
             int64_t g = -1, d = -1;
             if (lane < nrows) {
                 g = a.src32 ? int64_t(a.src32[off + lane]) : a.src64[off + lane];
-                d = a.dst32 ? int64_t(a.dst32[off + lane]) : a.dst64[off + lane];
+                d = a.dst_by_entry ? off + lane
+                                   : (a.dst32 ? int64_t(a.dst32[off + lane]) : a.dst64[off + lane]);
             }
             const bool src_ok = g >= 0 && (a.src_limit < 0 || g < a.src_limit);
             const bool dst_ok = d >= 0 && (a.dst_limit < 0 || d < a.dst_limit);
@@ -202,7 +205,8 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 dp = int64_t(reinterpret_cast<uintptr_t>(dst_row(a, r, d)));
             }
             if (lane < nrows && !dst_ok && !(a.pad_dst && d == -1)) bad = true;
-            if (lane < nrows && dst_ok && !src_ok && (!a.zero_bad_src || a.dgi == nullptr))
+            if (lane < nrows && dst_ok && !src_ok && !a.skip_bad_src &&
+                (!a.zero_bad_src || a.dgi == nullptr))
                 bad = true;
             // Rows without a source: zero the destination and revoke the slot.
             unsigned zmask = __ballot_sync(0xffffffffu, lane < nrows && dst_ok && !src_ok &&
@@ -311,6 +315,38 @@ int launch_xfer(XferArgs a, int64_t max_items_rows, int max_ctas, hs_stream_t st
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// SwapIn's copy engine for rows that are reconstructed afterwards: entry m
+// of list r (m < miss_count[r]) is copied from host row miss_src[r][m] to
+// staging row r * cap + m; entries without a source row are skipped (the
+// reconstruction handles them).
+int hs_swap_in_staged(const void* host_pool, int64_t host_rows, void* staging,
+                      int64_t row_bytes, const int32_t* miss_src, const int32_t* miss_count,
+                      int32_t rows, int32_t cap, int32_t max_ctas, int32_t* ticket,
+                      int32_t* status, hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || host_rows < 0 || row_bytes <= 0 || max_ctas < 0)
+        return HS_ERR_INVALID_ARG;
+    if (row_bytes % 16 != 0) return HS_ERR_MISALIGNED;
+    if (row_bytes > int64_t(kStageBytes)) return HS_ERR_CAPACITY;
+    if (rows == 0 || cap == 0) return HS_OK;
+    if (!aligned16(host_pool) || !aligned16(staging)) return HS_ERR_MISALIGNED;
+    XferArgs a{};
+    a.src_base = static_cast<const uint8_t*>(host_pool);
+    a.dst_base = static_cast<uint8_t*>(staging);
+    a.row_bytes = row_bytes;
+    a.src_limit = host_rows;
+    a.dst_limit = int64_t(rows) * cap;
+    a.src32 = miss_src;
+    a.counts = miss_count;
+    a.nlists = rows;
+    a.list_stride = cap;
+    a.dst_by_entry = 1;
+    a.skip_bad_src = 1;
+    a.status = status;
+    a.timeout_ns = hs::kWaitTimeoutNs;
+    a.ticket = ticket;
+    return launch_xfer(a, int64_t(rows) * cap, max_ctas, stream);
+}
 
 extern "C" int hs_swap_in(const void* host_pool, int64_t host_rows, void* hot, int64_t row_bytes,
                           const int32_t* miss_src, const int64_t* miss_dst,

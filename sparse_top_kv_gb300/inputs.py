@@ -86,6 +86,19 @@ def fill_randn_bf16_pinned(rows, width, seed, chunk_rows=1 << 20):
     return out
 
 
+def fill_randn_fp8ds_pinned(rows, seed, chunk_rows=1 << 19):
+    """A pinned host tensor [rows, 656] uint8 of fp8_ds_mla rows encoding N(0,1)
+    values (fp8ds_encode), generated on the GPU in chunks and copied down."""
+    out = pinned_empty((rows, FP8DS_ROW_BYTES), torch.uint8)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1].copy_(fp8ds_encode(torch.randn(r1 - r0, 576, generator=g, device="cuda")))
+    torch.cuda.synchronize()
+    host_read_pass(out)
+    return out
+
+
 def page_table(num_reqs, pages_per_req, num_pages, seed):
     """Random physical pages: a permutation of the pool, dealt out to requests."""
     perm = _rng(seed).permutation(num_pages)[: num_reqs * pages_per_req]
@@ -138,7 +151,9 @@ def hisparse_index_steps(num_reqs, top_k, prefill, steps, keep, seed, zipf_s=Non
     return out
 
 
-def tiny_hisparse():
+def tiny_hisparse(row_format="bf16"):
+    """Config tiny_hisparse; row_format "fp8ds": the pool and the new rows as
+    fp8_ds_mla rows (the same values, encoded)."""
     seed = SEEDS["tiny_hisparse"]
     cfg = dict(name="tiny_hisparse", num_reqs=1, heads=16, d_qk=576, d_v=512, page_size=64,
                total_positions=1024, steps=4, top_k=64, hot_size=128, region_stride=129,
@@ -153,12 +168,19 @@ def tiny_hisparse():
     cfg["q"] = randn_bf16((cfg["steps"], 1, 16, 576), seed + 200)
     cfg["new_rows"] = randn_bf16((cfg["steps"], 1, 576), seed + 300)
     cfg["newest_pos"] = np.array([[cfg["prefill"] + s] for s in range(cfg["steps"])], np.int32)
+    cfg["row_format"] = row_format
+    if row_format == "fp8ds":
+        cfg["pool"] = fp8ds_encode(cfg["pool"].float())
+        cfg["new_rows"] = fp8ds_encode(cfg["new_rows"].float().reshape(-1, 576)).reshape(
+            cfg["steps"], 1, FP8DS_ROW_BYTES)
     return cfg
 
 
-def full_hisparse(steps=16, num_reqs=64, top_k=2048, heads=16, pool_on_gpu_seed=True):
+def full_hisparse(steps=16, num_reqs=64, top_k=2048, heads=16, pool_on_gpu_seed=True,
+                  row_format="bf16"):
     """Config full_hisparse.  The 9.66 GB pool is generated on the GPU and copied
-    into pinned host memory (requires CUDA)."""
+    into pinned host memory (requires CUDA).  row_format "fp8ds": the pool
+    (5.5 GB) and the new rows as fp8_ds_mla rows of N(0,1) values."""
     seed = SEEDS["full_hisparse"]
     B = 64
     total = 131072
@@ -170,12 +192,19 @@ def full_hisparse(steps=16, num_reqs=64, top_k=2048, heads=16, pool_on_gpu_seed=
                scale=1.0 / math.sqrt(576.0), seed=seed, num_pages=num_pages)
     cfg["prefill"] = total - steps
     cfg["block_table"] = page_table(num_reqs, pages_per_req, num_pages, seed)
-    cfg["pool"] = fill_randn_bf16_pinned(num_pages * B, 576, seed + 100)
+    if row_format == "fp8ds":
+        cfg["pool"] = fill_randn_fp8ds_pinned(num_pages * B, seed + 100)
+    else:
+        cfg["pool"] = fill_randn_bf16_pinned(num_pages * B, 576, seed + 100)
+    cfg["row_format"] = row_format
     cfg["cand"] = hisparse_index_steps(num_reqs, top_k, cfg["prefill"], steps,
                                        keep=round(0.85 * top_k), seed=seed, zipf_s=1.1)
     g = torch.Generator(device="cpu").manual_seed(seed + 200)
     cfg["q"] = torch.randn(steps, num_reqs, heads, 576, generator=g).to(torch.bfloat16)
     cfg["new_rows"] = torch.randn(steps, num_reqs, 576, generator=g).to(torch.bfloat16)
+    if row_format == "fp8ds":
+        cfg["new_rows"] = fp8ds_encode(cfg["new_rows"].float().reshape(-1, 576)).reshape(
+            steps, num_reqs, FP8DS_ROW_BYTES)
     cfg["newest_pos"] = np.array([[cfg["prefill"] + s] * num_reqs for s in range(steps)],
                                  np.int32)
     return cfg

@@ -18,17 +18,30 @@ from . import hs
 class HiSparseDecoder:
     """Per-layer hot buffer of `num_reqs` regions of `region_stride` rows of
     `row_width` bf16 elements, backed by a pinned host pool (the only
-    full-size store, keyed by global slot id)."""
+    full-size store, keyed by global slot id).
+
+    row_format "fp8ds": the pool holds fp8_ds_mla rows (uint8 [rows, 656],
+    vLLM HiSparse walkthrough's FP8_DS_MLA_ROW_BYTES), and so do the new rows
+    a step receives; the hot buffer holds their bf16 reconstruction (576
+    columns), made as the SwapIn copies a row in (hs_swap_in_fp8ds), so the
+    host link carries 656 bytes per miss and the attention is unchanged."""
 
     def __init__(self, *, host_pool, block_table, num_pages, page_size, top_k, hot_size,
                  region_stride, heads, d_qk=576, d_v=512, scale, window=0, num_sinks=0,
-                 device="cuda"):
+                 device="cuda", row_format="bf16"):
         if not host_pool.is_pinned():
             raise ValueError("host pool must be pinned")
+        if row_format not in ("bf16", "fp8ds"):
+            raise ValueError("row_format: bf16 or fp8ds")
+        self.fp8 = row_format == "fp8ds"
+        if self.fp8 and (host_pool.dtype != torch.uint8 or host_pool.shape[1] < hs.FP8DS_ROW_BYTES
+                         or d_qk != 576):
+            raise ValueError("fp8ds: host pool uint8 [rows, >= 656], MLA rows (d_qk 576)")
         self.device = torch.device(device)
         self.num_reqs = block_table.shape[0]
-        self.row_width = host_pool.shape[1]
-        self.row_bytes = self.row_width * host_pool.element_size()
+        self.row_width = d_qk if self.fp8 else host_pool.shape[1]
+        # Bytes of one pool row (what the host link and the BackUp move).
+        self.row_bytes = host_pool.shape[1] * host_pool.element_size()
         self.host_pool = host_pool
         self.host_rows = host_pool.shape[0]
         self.host_dev = hs.host_device_pointer(host_pool)
@@ -39,7 +52,8 @@ class HiSparseDecoder:
         self.window, self.num_sinks = window, num_sinks
         R = self.num_reqs
         dev = self.device
-        self.hot = torch.zeros(R * region_stride, self.row_width, dtype=host_pool.dtype, device=dev)
+        self.hot = torch.zeros(R * region_stride, self.row_width,
+                               dtype=torch.bfloat16 if self.fp8 else host_pool.dtype, device=dev)
         self.dgi = torch.empty(R, hot_size, dtype=torch.int32, device=dev)
         self.lru = torch.empty(R, hot_size, dtype=torch.int16, device=dev)
         hs.hot_state_reset(self.dgi, self.lru)
@@ -48,6 +62,17 @@ class HiSparseDecoder:
         self.row_req = torch.arange(R, dtype=torch.int32, device=dev)
         self.reserved_rows = (torch.arange(R, dtype=torch.int64, device=dev) * region_stride
                               + hot_size)
+        if self.fp8:
+            # The new rows' reconstruction into the reserved rows: row r of
+            # the step's new-row buffer -> reserved row r.
+            self.new_src = torch.arange(R, dtype=torch.int32, device=dev).view(R, 1)
+            self.new_dst = self.reserved_rows.view(R, 1).clone()
+            self.new_cnt = torch.ones(R, dtype=torch.int32, device=dev)
+            self.new_rows_idx = torch.arange(R, dtype=torch.int64, device=dev)
+            # The misses cross the link through SwapIn's copy engine into this
+            # staging list, then every SM reconstructs them into their hot rows.
+            self.staging = torch.empty(R * (top_k + window + num_sinks) * self.row_bytes,
+                                       dtype=torch.uint8, device=dev)
         cap = top_k + window + num_sinks
         self.cap = cap
         i32 = dict(dtype=torch.int32, device=dev)
@@ -85,6 +110,7 @@ class HiSparseDecoder:
         attn_ctas = R * max(1, heads // hg) * max(1, self.parts_hit)
         self.swap_ctas = max(16, sms - attn_ctas)
 
+
     def warm_pool(self, page_bytes=4096):
         """One-time set-up pass: read one row of every `page_bytes` of the host
         pool (every 4 KB page by default) into the (still empty) hot buffer
@@ -107,8 +133,12 @@ class HiSparseDecoder:
             src = src.view(1, n).contiguous()
             dst = torch.arange(n, dtype=torch.int64, device=self.device).view(1, n)
             cnt = torch.full((1,), n, dtype=torch.int32, device=self.device)
-            hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, src, dst, cnt,
-                       status=self.status)
+            if self.fp8:
+                hs.swap_in_fp8ds(self.host_dev, self.host_rows, self.row_bytes, self.hot, src,
+                                 dst, cnt, status=self.status)
+            else:
+                hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, src, dst,
+                           cnt, status=self.status)
         self.hot.zero_()
         torch.cuda.synchronize(self.device)
 
@@ -122,7 +152,8 @@ class HiSparseDecoder:
     def step(self, cand, seq_lens, newest_slot, new_row, q, stream=None, events=None,
              out=None, lse=None):
         """cand int32 [R, top_k] positions; seq_lens int32 [R]; newest_slot int32
-        [R]; new_row [R, row_width] (the new token's KV row); q bf16 [R, H, d_qk].
+        [R]; new_row [R, row_width] (the new token's KV row; uint8 [R, 656]
+        fp8_ds_mla rows with row_format "fp8ds"); q bf16 [R, H, d_qk].
         Returns (out bf16 [R, H, d_v], lse fp32 [R, H]); state is updated.
         cand, seq_lens and newest_slot may be pinned host tensors (the kernels
         read them over the link); `out` / `lse`, if given (device or pinned
@@ -158,10 +189,17 @@ class HiSparseDecoder:
         # the step's critical path and each may start (set-up only) while its
         # predecessor runs (programmatic dependent launch).
         rec(3, main)
-        hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src, miss_dst,
-                   miss_count, dgi=self.dgi, hot_size=self.hot_size,
-                   region_stride=self.region_stride, max_ctas=self.swap_ctas,
-                   ticket=self.ticket, status=self.status, stream=main)
+        if self.fp8:
+            hs.swap_in_fp8ds(self.host_dev, self.host_rows, self.row_bytes, self.hot, miss_src,
+                             miss_dst, miss_count, dgi=self.dgi, hot_size=self.hot_size,
+                             region_stride=self.region_stride, staging=self.staging,
+                             max_ctas=self.swap_ctas, ticket=self.ticket, status=self.status,
+                             stream=main)
+        else:
+            hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src,
+                       miss_dst, miss_count, dgi=self.dgi, hot_size=self.hot_size,
+                       region_stride=self.region_stride, max_ctas=self.swap_ctas,
+                       ticket=self.ticket, status=self.status, stream=main)
         rec(4, main)
         # Side stream, once S2 has listed the misses (kernels beside S1 and
         # S2 slowed them by ~5 us in the captured step, measured): the
@@ -174,12 +212,23 @@ class HiSparseDecoder:
         qv = self.q_view(q)
         nkv = self.hot.shape[0]
         side.wait_event(self.ev_lists)
-        with torch.cuda.stream(side):
-            self.hot.index_copy_(0, self.reserved_rows, new_row)
+        if self.fp8:
+            # fp8 rows: the new rows are reconstructed into the reserved rows
+            # and backed up in their 656-byte form.
+            hs.swap_in_fp8ds(hs.device_address(new_row), self.num_reqs, self.row_bytes, self.hot,
+                             self.new_src, self.new_dst, self.new_cnt, status=self.status,
+                             stream=side)
+        else:
+            with torch.cuda.stream(side):
+                self.hot.index_copy_(0, self.reserved_rows, new_row)
         if not torch.cuda.is_current_stream_capturing():
             new_row.record_stream(side)  # the caller's tensor is read on the side stream
-        hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
-                  self.host_rows, status=self.status, stream=side)
+        if self.fp8:
+            hs.backup(new_row, self.new_rows_idx, self.host_dev, newest_slot, self.row_bytes,
+                      self.host_rows, status=self.status, stream=side)
+        else:
+            hs.backup(self.hot, self.reserved_rows, self.host_dev, newest_slot, self.row_bytes,
+                      self.host_rows, status=self.status, stream=side)
         hs.sparse_decode_partial(qv, self.hot, self.hot, self.row_width, 0, nkv,
                                  hit_idx.view(R, 1, self.cap), count.view(R, 1), self.scale,
                                  self.d_v, self.part_m, self.part_l, self.part_o, 0,
@@ -202,8 +251,10 @@ class HiSparseDecoder:
         """Byte layout of one step's inputs packed in one buffer: (name,
         offset, shape, dtype) per input, 256-byte aligned."""
         R = self.num_reqs
+        new_row = ((R, self.row_bytes), torch.uint8) if self.fp8 else ((R, self.row_width),
+                                                                        self.hot.dtype)
         specs = [("cand", (R, self.top_k), torch.int32), ("seq", (R,), torch.int32),
-                 ("newest", (R,), torch.int32), ("new_row", (R, self.row_width), self.hot.dtype),
+                 ("newest", (R,), torch.int32), ("new_row",) + new_row,
                  ("q", (R, self.heads, self.d_qk), torch.bfloat16)]
         out, off = [], 0
         for name, shape, dt in specs:

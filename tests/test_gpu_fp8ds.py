@@ -209,3 +209,43 @@ def test_swap_in_and_backup_of_656_byte_rows():
     torch.cuda.synchronize()
     before[bdst] = exp[brows]
     np.testing.assert_array_equal(pool.numpy(), before)
+
+
+@pytest.mark.parametrize("max_ctas,staged", [(0, False), (8, False), (0, True), (4, True)])
+def test_swap_in_fp8ds_matches_oracle(max_ctas, staged):
+    """Reconstructing SwapIn from a pinned fp8_ds_mla pool into bf16 hot rows,
+    in one kernel or through the copy engine and a staging list: whole hot
+    buffer and dgi byte for byte against the oracle, with contiguous runs,
+    scattered rows, a source outside the pool (zeroed, slot revoked) and a
+    ragged count."""
+    rng = np.random.default_rng(60 + max_ctas)
+    pool_rows, R, M, hot_size = 4000, 5, 257, 300
+    region = hot_size + 1
+    pool = torch.from_numpy(random_fp8_rows(rng, pool_rows)).pin_memory()
+    src = np.stack([np.sort(rng.choice(pool_rows, M, replace=False)) for _ in range(R)])
+    src[0] = np.arange(1000, 1000 + M)
+    src = src.astype(np.int32)
+    src[2, 17] = pool_rows + 5
+    dst = np.stack([r * region + rng.permutation(hot_size)[:M] for r in range(R)]).astype(
+        np.int64)
+    cnt = np.array([M, 0, 200, 1, 131], np.int32)
+    dgi0 = rng.integers(0, 1 << 20, (R, hot_size)).astype(np.int32)
+    hot_np = rng.integers(0, 1 << 16, (R * region, 576), dtype=np.uint16)
+    hot = torch.from_numpy(hot_np.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    dgi = cuda(dgi0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    staging = torch.empty(R * M * RB, dtype=torch.uint8, device="cuda") if staged else None
+    ticket = torch.zeros(2, dtype=torch.int32, device="cuda") if staged else None
+    hs.swap_in_fp8ds(hs.host_device_pointer(pool), pool_rows, RB, hot, cuda(src), cuda(dst),
+                     cuda(cnt), dgi=dgi, hot_size=hot_size, region_stride=region,
+                     staging=staging, max_ctas=max_ctas, ticket=ticket, status=status)
+    torch.cuda.synchronize()
+    exp = hot_np.copy()
+    dgi_exp = dgi0.copy()
+    oracle.swap_in_fp8ds(pool.numpy(), exp, src, dst, cnt, dgi=dgi_exp, hot_size=hot_size,
+                         region_stride=region)
+    np.testing.assert_array_equal(bits(hot), exp)
+    np.testing.assert_array_equal(np_i32(dgi), dgi_exp)
+    assert status.item() == 0
+    if ticket is not None:
+        assert (np_i32(ticket) == 0).all()

@@ -17,18 +17,20 @@ pytestmark = pytest.mark.gpu
 def run_steps(cfg, pool, attend_sample=None, steps=None):
     R = cfg["num_reqs"]
     B = cfg["page_size"]
-    rb = 576 * 2
+    fmt = cfg.get("row_format", "bf16")
+    rb = pool.shape[1] * pool.element_size()  # bytes of a pool row (and of a new row)
     dec = HiSparseDecoder(host_pool=pool, block_table=torch.from_numpy(cfg["block_table"]),
                           num_pages=cfg["num_pages"], page_size=B, top_k=cfg["top_k"],
                           hot_size=cfg["hot_size"], region_stride=cfg["region_stride"],
-                          heads=cfg["heads"], scale=cfg["scale"])
+                          heads=cfg["heads"], scale=cfg["scale"], row_format=fmt)
     # The oracle reads the same pinned pool: both sides write identical
     # BackUp rows, and step s only reads positions < T_s, which no later
     # BackUp overwrites.
     ora = OracleHiSparse(host_pool_u8=pool.view(torch.uint8).numpy(),
                          block_table=cfg["block_table"], num_pages=cfg["num_pages"],
                          page_size=B, top_k=cfg["top_k"], hot_size=cfg["hot_size"],
-                         region_stride=cfg["region_stride"], row_bytes=rb, scale=cfg["scale"])
+                         region_stride=cfg["region_stride"], row_bytes=rb, scale=cfg["scale"],
+                         row_format=fmt)
     hit_rates = []
     nsteps = cfg["steps"] if steps is None else steps
     for s in range(nsteps):
@@ -82,6 +84,23 @@ def test_tiny_hisparse_all_steps():
     run_steps(cfg, pool)
 
 
+def test_tiny_hisparse_fp8_all_steps():
+    """fp8_ds_mla pool and new rows: the hot buffer holds their bf16
+    reconstruction, compared byte for byte with the oracle's every step."""
+    cfg = inputs.tiny_hisparse("fp8ds")
+    pool = cfg["pool"].pin_memory()
+    run_steps(cfg, pool)
+
+
+def test_full_hisparse_fp8_steps_sampled_attention():
+    """The full-size step with the 5.5 GB fp8_ds_mla pool: six steps, S1-S3,
+    the reconstructed hot buffer, the pool and the state compared in full,
+    S4 on two sampled requests per step."""
+    cfg = inputs.full_hisparse(row_format="fp8ds")
+    rates = run_steps(cfg, cfg["pool"], attend_sample=[0, 63], steps=6)
+    assert rates[0] == 0.0 and min(rates[1:]) > 0.5
+
+
 def test_full_hisparse_all_steps_sampled_attention():
     """64 requests, context 131072, top_k 2048, hot 4097 rows, the pinned
     9.66 GB pool; S1-S3 and the state compared in full at every step, S4 on
@@ -91,14 +110,15 @@ def test_full_hisparse_all_steps_sampled_attention():
     assert rates[0] == 0.0 and min(rates[1:]) > 0.5
 
 
-def test_captured_step_matches_eager():
+@pytest.mark.parametrize("row_format", ["bf16", "fp8ds"])
+def test_captured_step_matches_eager(row_format):
     """The captured step, replayed with a staged copy of the inputs
     (replay_packed), as one graph per input slot read in place
     (capture(slot=...)) and as one graph per pinned host input buffer with
     the results copied back to pinned host tensors (host_in / host_out),
     gives the eager step's outputs and state bit for bit at every step (the
     decoders write identical BackUp rows into the shared pool)."""
-    cfg = inputs.tiny_hisparse()
+    cfg = inputs.tiny_hisparse(row_format)
     pool = cfg["pool"].pin_memory()
     R = cfg["num_reqs"]
 
@@ -107,7 +127,7 @@ def test_captured_step_matches_eager():
                                num_pages=cfg["num_pages"], page_size=cfg["page_size"],
                                top_k=cfg["top_k"], hot_size=cfg["hot_size"],
                                region_stride=cfg["region_stride"], heads=cfg["heads"],
-                               scale=cfg["scale"])
+                               scale=cfg["scale"], row_format=row_format)
 
     decs = [make(), make(), make(), make()]
     steps = []

@@ -132,3 +132,36 @@ def test_attention_on_fp8_rows_matches_brute_force():
             np.testing.assert_allclose(out[r, h], p @ K[:, :512] / p.sum(), rtol=1e-12,
                                        atol=1e-12)
             assert abs(lse[r, h] - (m + math.log(p.sum()))) < 1e-12
+
+
+def test_swap_in_fp8ds_is_byte_swap_then_reconstruction():
+    """The reconstructing SwapIn equals the byte-level SwapIn of the 656-byte
+    rows into a staging buffer followed by fp8ds_dequant of the staged rows;
+    a source outside the pool zeroes the hot row and revokes its slot."""
+    rng = np.random.default_rng(13)
+    host_rows, R, region, hot_size = 50, 2, 9, 8
+    vals = torch.from_numpy(rng.standard_normal((host_rows, 576)).astype(np.float32))
+    from sparse_top_kv_gb300 import inputs
+    pool = inputs.fp8ds_encode(vals).numpy()
+    msrc = np.array([[3, 49, 7, 0], [12, -1, 30, 0]], np.int32)
+    mdst = np.array([[0, 5, 2, 0], [9 + 1, 9 + 4, 9 + 7, 0]], np.int64)
+    mcount = np.array([3, 3], np.int32)
+    hot = rng.integers(0, 1 << 16, (R * region, 576), dtype=np.uint16)
+    expect = hot.copy()
+    dgi = np.arange(R * hot_size, dtype=np.int32).reshape(R, hot_size)
+    dgi_exp = dgi.copy()
+    oracle.swap_in_fp8ds(pool, hot, msrc, mdst, mcount, dgi=dgi, hot_size=hot_size,
+                         region_stride=region)
+    staged = np.zeros((R * region, 656), np.uint8)
+    oracle.swap_in(pool.reshape(-1), staged.reshape(-1), 656,
+                   np.where(msrc >= 0, msrc, 0), mdst, mcount)
+    for r in range(R):
+        for m in range(mcount[r]):
+            d = mdst[r, m]
+            if msrc[r, m] >= 0:
+                expect[d] = oracle.fp8ds_dequant(staged, [d])[0]
+            else:
+                expect[d] = 0
+                dgi_exp[r, d - r * region] = -1
+    np.testing.assert_array_equal(hot, expect)
+    np.testing.assert_array_equal(dgi, dgi_exp)
