@@ -582,6 +582,7 @@ def bench_full_fp8(args, flush):
            "stage_us": {"s1": st[0] * 1e3, "s2": st[1] * 1e3, "swap_in": st[3] * 1e3,
                         "resident_rows": st[4] * 1e3, "swapped_rows_merge": st[5] * 1e3},
            "swap_in_gbs": r["swap_bytes_per_step"] / (st[3] * 1e6) if st[3] > 0 else None,
+           "step_us_timed": [round(x * 1e3, 1) for x in r["step_ms"]],
            "clocks": r["clocks"]}
     del r
     return out

@@ -420,32 +420,25 @@ int hs_fp8ds_gather(const void* kv8, int64_t row_bytes, int64_t num_kv_rows,
 /* ---------------------------------------------------------------------------
  * hs_swap_in_fp8ds -- S3 SwapIn ([HS] Phase 5) for a host pool of
  * fp8_ds_mla rows and a hot buffer of reconstructed bf16 rows: every miss row
- * crosses the host link in its 656-byte form and is reconstructed (as in
- * hs_fp8ds_gather) on its way into the hot row, so the attention reads the
- * hot buffer as bf16 MLA rows (576 columns).
- * host_pool8  device-visible pointer to the pinned pool, host_rows rows
- *             host_row_bytes apart (>= 656, multiple of 16, 16-byte aligned).
+ * crosses the host link in its 656-byte form (hs_swap_in's staged copy), and
+ * the copy's store step writes its reconstruction (as in hs_fp8ds_gather) to
+ * the hot row, so the attention reads the hot buffer as bf16 MLA rows (576
+ * columns).
+ * host_pool8  device-visible pointer to the pinned pool (or a device
+ *             buffer), host_rows rows host_row_bytes apart (>= 656, multiple
+ *             of 16, 16-byte aligned).
  * hot         device bf16 rows of 576 (1152 B), hot_rows rows.
- * miss_src/miss_dst/miss_count/rows/cap/dgi/hot_size/region_stride as for
- *             hs_swap_in: a source outside [0, host_rows) zeroes the hot row
- *             and revokes its slot (dgi = -1; HS_ERR_BAD_INDEX without dgi); a
- *             destination outside [0, hot_rows) is skipped with
- *             HS_ERR_BAD_INDEX.  Destinations must be distinct within a call.
- * staging     NULL: one kernel reads the source rows itself (register-staged
- *             loads; meant for device-resident sources and small counts;
- *             max_ctas CTAs, up to 3 per SM, 0 = every SM).  Otherwise a
- *             device buffer of at least rows * cap * host_row_bytes bytes
- *             (staging_bytes), 16-byte aligned: the rows cross the link
- *             through hs_swap_in's copy engine (max_ctas SMs, `ticket` as
- *             there) into staging row r * cap + m, then a second launch on
- *             every SM reconstructs them into the hot rows.
+ * miss_src/miss_dst/miss_count/rows/cap/dgi/hot_size/region_stride/max_ctas/
+ * ticket      as for hs_swap_in: a source outside [0, host_rows) zeroes the
+ *             hot row and revokes its slot (dgi = -1; HS_ERR_BAD_INDEX
+ *             without dgi); a destination outside [0, hot_rows) is skipped
+ *             with HS_ERR_BAD_INDEX.  Destinations must be distinct.
  * ------------------------------------------------------------------------- */
 int hs_swap_in_fp8ds(const void* host_pool8, int64_t host_rows, int64_t host_row_bytes,
                      void* hot, int64_t hot_rows, const int32_t* miss_src,
                      const int64_t* miss_dst, const int32_t* miss_count, int32_t rows,
                      int32_t cap, int32_t* dgi, int32_t hot_size, int64_t region_stride,
-                     void* staging, int64_t staging_bytes, int32_t max_ctas, int32_t* ticket,
-                     int32_t* status, hs_stream_t stream);
+                     int32_t max_ctas, int32_t* ticket, int32_t* status, hs_stream_t stream);
 
 int64_t hs_sparse_decode_fp8ds_workspace_bytes(int32_t rows, int32_t heads, int32_t cap);
 

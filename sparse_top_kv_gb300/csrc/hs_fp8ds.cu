@@ -46,20 +46,7 @@ struct GatherArgs {
     int32_t rows;
     int32_t cap;
     __nv_bfloat16* out;      // bf16 rows of 576
-    int32_t* out_ids;        // gather: [rows * cap], r * cap + j or -1 (no row); or null
-    // SwapIn (out_rows != null): entry (r, j) goes to out row out_rows[r][j]
-    // (< out_limit); a source outside the rows zeroes that row and revokes
-    // its hot slot in dgi (or is an error without dgi).  Gather (null): to
-    // out row r * cap + j; a negative id is no row, an id past the rows an
-    // error.
-    const int64_t* out_rows;
-    int64_t out_limit;
-    int32_t* dgi;
-    int32_t hot_size;
-    int64_t region_stride;
-    // 1: entry f's row was staged at row f of kv8 (its id only decides
-    // whether it has a source row, against num_kv_rows).
-    int32_t staged;
+    int32_t* out_ids;        // [rows * cap]: r * cap + j, or -1 (no row)
     int32_t* status;
 };
 
@@ -95,10 +82,10 @@ __global__ void __launch_bounds__(kThreads, 3) fp8ds_gather_kernel(const GatherA
                 }
             }
             const bool v = live[u] && id[u] >= 0 && int64_t(id[u]) < a.num_kv_rows;
-            if (live[u] && !a.out_rows && int64_t(id[u]) >= a.num_kv_rows) bad = true;
+            if (live[u] && int64_t(id[u]) >= a.num_kv_rows) bad = true;
             if (!v) id[u] = -1;
             if (id[u] >= 0) {
-                const unsigned char* row = a.kv8 + (a.staged ? f : int64_t(id[u])) * a.row_bytes;
+                const unsigned char* row = a.kv8 + int64_t(id[u]) * a.row_bytes;
                 lo[u] = __ldg(reinterpret_cast<const uint2*>(row) + lane);
                 hi[u] = __ldg(reinterpret_cast<const uint2*>(row + 256) + lane);
                 const float* sc = reinterpret_cast<const float*>(row + 512);
@@ -111,32 +98,9 @@ __global__ void __launch_bounds__(kThreads, 3) fp8ds_gather_kernel(const GatherA
         for (int u = 0; u < kRowsPerWarp; ++u) {
             const int64_t f = base + u;
             if (!live[u]) continue;
-            int64_t d = f;
-            if (a.out_rows) {
-                d = __ldg(a.out_rows + f);
-                if (d < 0 || d >= a.out_limit) {
-                    bad = true;
-                    continue;
-                }
-                if (id[u] < 0) {
-                    // No source row: zero the hot row and revoke its slot.
-                    uint4* z = reinterpret_cast<uint4*>(a.out + d * 576);
-                    z[lane] = make_uint4(0, 0, 0, 0);
-                    z[32 + lane] = make_uint4(0, 0, 0, 0);
-                    if (lane < 8) z[64 + lane] = make_uint4(0, 0, 0, 0);
-                    const int r = int(f / a.cap);
-                    const int64_t sl = d - int64_t(r) * a.region_stride;
-                    if (a.dgi == nullptr)
-                        bad = true;
-                    else if (lane == 0 && sl >= 0 && sl < a.hot_size)
-                        a.dgi[int64_t(r) * a.hot_size + sl] = -1;
-                    continue;
-                }
-            } else if (a.out_ids != nullptr && lane == 0) {
-                a.out_ids[f] = id[u] >= 0 ? int32_t(f) : -1;
-            }
+            if (lane == 0) a.out_ids[f] = id[u] >= 0 ? int32_t(f) : -1;
             if (id[u] < 0) continue;
-            uint4* dst = reinterpret_cast<uint4*>(a.out + d * 576);
+            uint4* dst = reinterpret_cast<uint4*>(a.out + f * 576);
             dst[lane] = hs::fp8_dequant8(lo[u], s_lo[u]);
             dst[32 + lane] = hs::fp8_dequant8(hi[u], s_hi[u]);
             if (lane < 8) dst[64 + lane] = rope[u];
@@ -167,20 +131,14 @@ int gather_ctas_per_sm() {
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 // Grid: enough warps for every entry, at most the resident CTAs of all SMs
-// (or max_ctas CTAs when given).  pdl = false: a plain launch, whose CTAs
-// take SMs only once the stream predecessor has finished (early CTAs waiting
-// on every SM would keep a concurrent kernel on another stream off them).
-int launch_gather(const GatherArgs& a, int64_t total, int32_t max_ctas, hs_stream_t stream,
-                  bool pdl = true) {
+// (or max_ctas CTAs when given).
+int launch_gather(const GatherArgs& a, int64_t total, int32_t max_ctas, hs_stream_t stream) {
     const int64_t warps = (total + kRowsPerWarp - 1) / kRowsPerWarp;
     int64_t ctas = hs::min64((warps * 32 + kThreads - 1) / kThreads,
                              int64_t(hs_host::num_sms()) * gather_ctas_per_sm());
     if (max_ctas > 0) ctas = hs::min64(ctas, max_ctas);
-    if (pdl)
-        return hs_host::launch_pdl(fp8ds_gather_kernel, dim3(unsigned(ctas)), dim3(kThreads), 0,
-                                   stream, a);
-    fp8ds_gather_kernel<<<unsigned(ctas), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return hs_host::launch_status();
+    return hs_host::launch_pdl(fp8ds_gather_kernel, dim3(unsigned(ctas)), dim3(kThreads), 0,
+                               stream, a);
 }
 
 }  // namespace
@@ -200,53 +158,8 @@ extern "C" int hs_fp8ds_gather(const void* kv8, int64_t row_bytes, int64_t num_k
     if ((reinterpret_cast<uintptr_t>(kv8) | reinterpret_cast<uintptr_t>(out)) & 15u)
         return HS_ERR_MISALIGNED;
     const GatherArgs a{static_cast<const unsigned char*>(kv8), row_bytes, num_kv_rows, kv_rows,
-                       count, rows, cap, static_cast<__nv_bfloat16*>(out), out_ids, nullptr, 0,
-                       nullptr, 0, 0, 0, status};
+                       count, rows, cap, static_cast<__nv_bfloat16*>(out), out_ids, status};
     return launch_gather(a, total, 0, stream);
-}
-
-// SwapIn's copy engine into a staging list (hs_transfer.cu).
-int hs_swap_in_staged(const void* host_pool, int64_t host_rows, void* staging,
-                      int64_t row_bytes, const int32_t* miss_src, const int32_t* miss_count,
-                      int32_t rows, int32_t cap, int32_t max_ctas, int32_t* ticket,
-                      int32_t* status, hs_stream_t stream);
-
-extern "C" int hs_swap_in_fp8ds(const void* host_pool8, int64_t host_rows, int64_t host_row_bytes,
-                                void* hot, int64_t hot_rows, const int32_t* miss_src,
-                                const int64_t* miss_dst, const int32_t* miss_count, int32_t rows,
-                                int32_t cap, int32_t* dgi, int32_t hot_size,
-                                int64_t region_stride, void* staging, int64_t staging_bytes,
-                                int32_t max_ctas, int32_t* ticket, int32_t* status,
-                                hs_stream_t stream) {
-    if (rows < 0 || cap < 0 || host_rows < 0 || hot_rows < 0 || max_ctas < 0 ||
-        host_row_bytes < kFp8RowBytes)
-        return HS_ERR_INVALID_ARG;
-    if (host_row_bytes % 16) return HS_ERR_MISALIGNED;
-    const int64_t total = int64_t(rows) * cap;
-    if (total == 0) return HS_OK;
-    if (total > INT32_MAX) return HS_ERR_CAPACITY;
-    if (host_pool8 == nullptr || hot == nullptr || miss_src == nullptr || miss_dst == nullptr ||
-        miss_count == nullptr || (dgi != nullptr && (hot_size <= 0 || region_stride < 0)))
-        return HS_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(host_pool8) | reinterpret_cast<uintptr_t>(hot)) & 15u)
-        return HS_ERR_MISALIGNED;
-    if (staging != nullptr) {
-        // The rows cross the link through the copy engine (max_ctas SMs),
-        // then every SM reconstructs them from the staging list.
-        if (staging_bytes < total * host_row_bytes) return HS_ERR_CAPACITY;
-        if (reinterpret_cast<uintptr_t>(staging) & 15u) return HS_ERR_MISALIGNED;
-        const int rc = hs_swap_in_staged(host_pool8, host_rows, staging, host_row_bytes, miss_src,
-                                         miss_count, rows, cap, max_ctas, ticket, status, stream);
-        if (rc != HS_OK) return rc;
-        const GatherArgs a{static_cast<const unsigned char*>(staging), host_row_bytes, host_rows,
-                           miss_src, miss_count, rows, cap, static_cast<__nv_bfloat16*>(hot),
-                           nullptr, miss_dst, hot_rows, dgi, hot_size, region_stride, 1, status};
-        return launch_gather(a, total, 0, stream, false);
-    }
-    const GatherArgs a{static_cast<const unsigned char*>(host_pool8), host_row_bytes, host_rows,
-                       miss_src, miss_count, rows, cap, static_cast<__nv_bfloat16*>(hot),
-                       nullptr, miss_dst, hot_rows, dgi, hot_size, region_stride, 0, status};
-    return launch_gather(a, total, max_ctas, stream);
 }
 
 extern "C" int64_t hs_sparse_decode_fp8ds_workspace_bytes(int32_t rows, int32_t heads,

@@ -25,7 +25,13 @@
 // scattered slots, and plain stores need no completion tracking), two groups
 // behind the loads so that three stages stay in flight per warp.  The
 // mbarrier waits are bounded in wall time (HS_ERR_TIMEOUT on expiry).
+//
+// fp8_ds_mla rows (hs_swap_in_fp8ds): the 656-byte rows cross the link as
+// they are and the store step writes each staged row's bf16 reconstruction
+// (1152 bytes: E4M3 code x fp32 group scale, rounded to bf16; RoPE copied)
+// to its hot row, so the hot buffer is read by the attention as bf16 rows.
 #include "hs_common.cuh"
+#include "hs_fp8.cuh"
 
 namespace {
 
@@ -58,8 +64,8 @@ struct XferArgs {
     int32_t* dgi;           // swap-in revocation target, or nullptr
     int32_t zero_bad_src;   // 1: a missing source zeroes the destination (SwapIn)
     int32_t pad_dst;        // 1: a destination id of -1 is padding, skipped silently (BackUp)
-    int32_t dst_by_entry;   // 1: entry m of list r goes to row r * list_stride + m (staging)
-    int32_t skip_bad_src;   // 1: an entry without a source row is skipped silently
+    int32_t fp8_rows;       // 1: sources are fp8_ds_mla rows, destinations bf16 rows of 576
+    int64_t dst_row_bytes;  // bytes per destination row (row_bytes unless fp8_rows)
     int32_t hot_size;
     int64_t region_stride;
     int32_t* status;
@@ -109,7 +115,7 @@ __device__ __forceinline__ const uint8_t* src_row(const XferArgs& a, int r, int6
     return host_row(a, r / a.layers, r % a.layers, id);
 }
 __device__ __forceinline__ uint8_t* dst_row(const XferArgs& a, int r, int64_t id) {
-    if (!a.layer_mode) return a.dst_base + id * a.row_bytes;
+    if (!a.layer_mode) return a.dst_base + id * a.dst_row_bytes;
     if (a.to_host) return host_row(a, r / a.layers, r % a.layers, id);
     return a.dev_layers[r] + id * a.row_bytes;
 }
@@ -124,7 +130,17 @@ __device__ __forceinline__ void store_group(const XferArgs& a, const WarpRing& R
         if (d < 0) continue;
         const uint4* src = reinterpret_cast<const uint4*>(stage + int64_t(k) * rb);
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uintptr_t>(d));
-        for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+        if (a.fp8_rows) {
+            // Lane l: the 16 codes of latent columns 16 l .. 16 l + 15 (scale
+            // group l / 8) -> 32 bf16 bytes; lanes 0-7: the RoPE bytes.
+            const uint4 c = src[lane];
+            const float sc = reinterpret_cast<const float*>(stage + int64_t(k) * rb + 512)[lane >> 3];
+            dst[2 * lane] = hs::fp8_dequant8(make_uint2(c.x, c.y), sc);
+            dst[2 * lane + 1] = hs::fp8_dequant8(make_uint2(c.z, c.w), sc);
+            if (lane < 8) dst[64 + lane] = src[33 + lane];
+        } else {
+            for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+        }
     }
 }
 
@@ -158,6 +174,8 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
     const int total = prefix[a.nlists];
     const int64_t rb = a.row_bytes;
     const int nv = int(rb / 16);
+    const int64_t drb = a.dst_row_bytes;  // destination row bytes
+    const int dnv = int(drb / 16);
     const int gw = blockIdx.x * kWarps + warp;   // global warp id
     const int nw = gridDim.x * kWarps;
     // Groups of this warp: round-robin over the grid, or, with a ticket
@@ -192,8 +210,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
             int64_t g = -1, d = -1;
             if (lane < nrows) {
                 g = a.src32 ? int64_t(a.src32[off + lane]) : a.src64[off + lane];
-                d = a.dst_by_entry ? off + lane
-                                   : (a.dst32 ? int64_t(a.dst32[off + lane]) : a.dst64[off + lane]);
+                d = a.dst32 ? int64_t(a.dst32[off + lane]) : a.dst64[off + lane];
             }
             const bool src_ok = g >= 0 && (a.src_limit < 0 || g < a.src_limit);
             const bool dst_ok = d >= 0 && (a.dst_limit < 0 || d < a.dst_limit);
@@ -205,8 +222,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 dp = int64_t(reinterpret_cast<uintptr_t>(dst_row(a, r, d)));
             }
             if (lane < nrows && !dst_ok && !(a.pad_dst && d == -1)) bad = true;
-            if (lane < nrows && dst_ok && !src_ok && !a.skip_bad_src &&
-                (!a.zero_bad_src || a.dgi == nullptr))
+            if (lane < nrows && dst_ok && !src_ok && (!a.zero_bad_src || a.dgi == nullptr))
                 bad = true;
             // Rows without a source: zero the destination and revoke the slot.
             unsigned zmask = __ballot_sync(0xffffffffu, lane < nrows && dst_ok && !src_ok &&
@@ -216,7 +232,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
                 zmask &= zmask - 1;
                 const int64_t dk = __shfl_sync(0xffffffffu, d, k);
                 uint4* z = reinterpret_cast<uint4*>(dst_row(a, r, dk));
-                for (int v = lane; v < nv; v += 32) z[v] = make_uint4(0, 0, 0, 0);
+                for (int v = lane; v < dnv; v += 32) z[v] = make_uint4(0, 0, 0, 0);
                 if (lane == 0 && a.dgi != nullptr) {
                     const int64_t s = dk - int64_t(r) * a.region_stride;
                     if (s >= 0 && s < a.hot_size) a.dgi[int64_t(r) * a.hot_size + s] = -1;
@@ -233,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const XferArgs a) {
             const int64_t sp0 = __shfl_sync(0xffffffffu, sp, 0);
             const int64_t dp0 = __shfl_sync(0xffffffffu, dp, 0);
             const bool in_run = !(lane < nrows) ||
-                                (copy && sp == sp0 + lane * rb && dp == dp0 + lane * rb);
+                                (copy && sp == sp0 + lane * rb && dp == dp0 + lane * drb);
             const bool one_run = nrows > 1 && cmask == ((nrows == 32) ? 0xffffffffu : ((1u << nrows) - 1u)) &&
                                  __all_sync(0xffffffffu, in_run);
             __syncwarp();
@@ -304,6 +320,7 @@ int launch_xfer(XferArgs a, int64_t max_items_rows, int max_ctas, hs_stream_t st
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(xfer_kernel), smem,
                                                 smem_set);
     if (rc != HS_OK) return rc;
+    if (a.dst_row_bytes == 0) a.dst_row_bytes = a.row_bytes;
     a.group = int32_t(hs::max64(1, hs::min64(kMaxGroup, int64_t(kStageBytes) / a.row_bytes)));
     const int64_t groups = (max_items_rows + a.group - 1) / a.group;
     // One CTA (192 KB of stages) per SM.
@@ -316,32 +333,40 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-// SwapIn's copy engine for rows that are reconstructed afterwards: entry m
-// of list r (m < miss_count[r]) is copied from host row miss_src[r][m] to
-// staging row r * cap + m; entries without a source row are skipped (the
-// reconstruction handles them).
-int hs_swap_in_staged(const void* host_pool, int64_t host_rows, void* staging,
-                      int64_t row_bytes, const int32_t* miss_src, const int32_t* miss_count,
-                      int32_t rows, int32_t cap, int32_t max_ctas, int32_t* ticket,
-                      int32_t* status, hs_stream_t stream) {
-    if (rows < 0 || cap < 0 || host_rows < 0 || row_bytes <= 0 || max_ctas < 0)
+extern "C" int hs_swap_in_fp8ds(const void* host_pool8, int64_t host_rows, int64_t host_row_bytes,
+                                void* hot, int64_t hot_rows, const int32_t* miss_src,
+                                const int64_t* miss_dst, const int32_t* miss_count, int32_t rows,
+                                int32_t cap, int32_t* dgi, int32_t hot_size,
+                                int64_t region_stride, int32_t max_ctas, int32_t* ticket,
+                                int32_t* status, hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || host_rows < 0 || hot_rows < 0 || max_ctas < 0 ||
+        host_row_bytes < 656)
         return HS_ERR_INVALID_ARG;
-    if (row_bytes % 16 != 0) return HS_ERR_MISALIGNED;
-    if (row_bytes > int64_t(kStageBytes)) return HS_ERR_CAPACITY;
+    if (host_row_bytes % 16 != 0) return HS_ERR_MISALIGNED;
+    if (host_row_bytes > int64_t(kStageBytes)) return HS_ERR_CAPACITY;
     if (rows == 0 || cap == 0) return HS_OK;
-    if (!aligned16(host_pool) || !aligned16(staging)) return HS_ERR_MISALIGNED;
+    if (host_pool8 == nullptr || hot == nullptr || miss_src == nullptr || miss_dst == nullptr ||
+        miss_count == nullptr)
+        return HS_ERR_INVALID_ARG;
+    if (!aligned16(host_pool8) || !aligned16(hot)) return HS_ERR_MISALIGNED;
+    if (dgi != nullptr && (hot_size <= 0 || region_stride < hot_size)) return HS_ERR_INVALID_ARG;
     XferArgs a{};
-    a.src_base = static_cast<const uint8_t*>(host_pool);
-    a.dst_base = static_cast<uint8_t*>(staging);
-    a.row_bytes = row_bytes;
+    a.src_base = static_cast<const uint8_t*>(host_pool8);
+    a.dst_base = static_cast<uint8_t*>(hot);
+    a.row_bytes = host_row_bytes;
+    a.fp8_rows = 1;
+    a.dst_row_bytes = 576 * 2;
     a.src_limit = host_rows;
-    a.dst_limit = int64_t(rows) * cap;
+    a.dst_limit = hot_rows;
     a.src32 = miss_src;
+    a.dst64 = miss_dst;
     a.counts = miss_count;
     a.nlists = rows;
     a.list_stride = cap;
-    a.dst_by_entry = 1;
-    a.skip_bad_src = 1;
+    a.dgi = dgi;
+    a.zero_bad_src = 1;
+    a.hot_size = hot_size;
+    a.region_stride = region_stride;
     a.status = status;
     a.timeout_ns = hs::kWaitTimeoutNs;
     a.ticket = ticket;

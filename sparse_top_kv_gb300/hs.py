@@ -58,8 +58,8 @@ _SIGS = {
                                   _I32, _I32, _F32, _P, _P, _P, _P], ctypes.c_int),
     "hs_fp8ds_gather": ([_P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P], ctypes.c_int),
     "hs_sparse_decode_fp8ds_workspace_bytes": ([_I32, _I32, _I32], _I64),
-    "hs_swap_in_fp8ds": ([_P, _I64, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _P,
-                          _I64, _I32, _P, _P, _P], ctypes.c_int),
+    "hs_swap_in_fp8ds": ([_P, _I64, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _I32,
+                          _P, _P, _P], ctypes.c_int),
     "hs_sparse_decode_fp8ds": ([_P, _P, _I64, _I64, _P, _P, _I32, _I32, _I32, _F32, _P, _P, _P,
                                 _I64, _P, _P], ctypes.c_int),
 }
@@ -321,26 +321,22 @@ def fp8ds_gather(kv8, kv_rows, count, *, out=None, out_ids=None, status=None, st
 
 
 def swap_in_fp8ds(host_pool_dev, host_rows, host_row_bytes, hot, miss_src, miss_dst,
-                  miss_count, *, dgi=None, hot_size=0, region_stride=0, staging=None,
-                  max_ctas=0, ticket=None, status=None, stream=None):
+                  miss_count, *, dgi=None, hot_size=0, region_stride=0, max_ctas=0,
+                  ticket=None, status=None, stream=None):
     """S3 SwapIn from a pool of fp8_ds_mla rows (device-visible address
-    host_pool_dev) into bf16 hot rows [hot_rows, 576], reconstructing on the
-    way.  staging: None (one kernel reads the rows itself) or a uint8 CUDA
-    tensor of at least rows * cap * host_row_bytes bytes (the rows cross the
-    link through the SwapIn copy engine first; `ticket` as for swap_in)."""
+    host_pool_dev) into bf16 hot rows [hot_rows, 576], reconstructing as the
+    copy stores each row; arguments as for swap_in."""
     _check(hot, torch.bfloat16, "hot")
-    _check(staging, torch.uint8, "staging")
-    _check(ticket, torch.int32, "ticket")
     _check(miss_src, torch.int32, "miss_src")
     _check(miss_dst, torch.int64, "miss_dst")
     _check(miss_count, torch.int32, "miss_count")
     _check(dgi, torch.int32, "dgi")
+    _check(ticket, torch.int32, "ticket")
     _check(status, torch.int32, "status")
     rows, cap = miss_src.shape
     _call("hs_swap_in_fp8ds", ctypes.c_void_p(host_pool_dev), host_rows, host_row_bytes,
           _ptr(hot), hot.shape[0], _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), rows, cap,
-          _ptr(dgi), hot_size, region_stride, _ptr(staging),
-          0 if staging is None else staging.numel(), max_ctas, _ptr(ticket), _ptr(status),
+          _ptr(dgi), hot_size, region_stride, max_ctas, _ptr(ticket), _ptr(status),
           _stream(stream))
 
 

@@ -23,7 +23,7 @@ class HiSparseDecoder:
     row_format "fp8ds": the pool holds fp8_ds_mla rows (uint8 [rows, 656],
     vLLM HiSparse walkthrough's FP8_DS_MLA_ROW_BYTES), and so do the new rows
     a step receives; the hot buffer holds their bf16 reconstruction (576
-    columns), made as the SwapIn copies a row in (hs_swap_in_fp8ds), so the
+    columns), written by the SwapIn's store step (hs_swap_in_fp8ds), so the
     host link carries 656 bytes per miss and the attention is unchanged."""
 
     def __init__(self, *, host_pool, block_table, num_pages, page_size, top_k, hot_size,
@@ -69,10 +69,6 @@ class HiSparseDecoder:
             self.new_dst = self.reserved_rows.view(R, 1).clone()
             self.new_cnt = torch.ones(R, dtype=torch.int32, device=dev)
             self.new_rows_idx = torch.arange(R, dtype=torch.int64, device=dev)
-            # The misses cross the link through SwapIn's copy engine into this
-            # staging list, then every SM reconstructs them into their hot rows.
-            self.staging = torch.empty(R * (top_k + window + num_sinks) * self.row_bytes,
-                                       dtype=torch.uint8, device=dev)
         cap = top_k + window + num_sinks
         self.cap = cap
         i32 = dict(dtype=torch.int32, device=dev)
@@ -192,9 +188,8 @@ class HiSparseDecoder:
         if self.fp8:
             hs.swap_in_fp8ds(self.host_dev, self.host_rows, self.row_bytes, self.hot, miss_src,
                              miss_dst, miss_count, dgi=self.dgi, hot_size=self.hot_size,
-                             region_stride=self.region_stride, staging=self.staging,
-                             max_ctas=self.swap_ctas, ticket=self.ticket, status=self.status,
-                             stream=main)
+                             region_stride=self.region_stride, max_ctas=self.swap_ctas,
+                             ticket=self.ticket, status=self.status, stream=main)
         else:
             hs.swap_in(self.host_dev, self.host_rows, self.hot, self.row_bytes, miss_src,
                        miss_dst, miss_count, dgi=self.dgi, hot_size=self.hot_size,
@@ -216,8 +211,8 @@ class HiSparseDecoder:
             # fp8 rows: the new rows are reconstructed into the reserved rows
             # and backed up in their 656-byte form.
             hs.swap_in_fp8ds(hs.device_address(new_row), self.num_reqs, self.row_bytes, self.hot,
-                             self.new_src, self.new_dst, self.new_cnt, status=self.status,
-                             stream=side)
+                             self.new_src, self.new_dst, self.new_cnt, max_ctas=0,
+                             status=self.status, stream=side)
         else:
             with torch.cuda.stream(side):
                 self.hot.index_copy_(0, self.reserved_rows, new_row)

@@ -211,13 +211,13 @@ def test_swap_in_and_backup_of_656_byte_rows():
     np.testing.assert_array_equal(pool.numpy(), before)
 
 
-@pytest.mark.parametrize("max_ctas,staged", [(0, False), (8, False), (0, True), (4, True)])
-def test_swap_in_fp8ds_matches_oracle(max_ctas, staged):
-    """Reconstructing SwapIn from a pinned fp8_ds_mla pool into bf16 hot rows,
-    in one kernel or through the copy engine and a staging list: whole hot
-    buffer and dgi byte for byte against the oracle, with contiguous runs,
-    scattered rows, a source outside the pool (zeroed, slot revoked) and a
-    ragged count."""
+@pytest.mark.parametrize("max_ctas,claim", [(0, False), (4, True), (24, True)])
+def test_swap_in_fp8ds_matches_oracle(max_ctas, claim):
+    """Reconstructing SwapIn from a pinned fp8_ds_mla pool into bf16 hot rows:
+    whole hot buffer and dgi byte for byte against the oracle, with contiguous
+    runs (one bulk load each), scattered rows, a source outside the pool
+    (zeroed, slot revoked) and a ragged count, on every SM or a budget, with
+    groups dealt round-robin or claimed by ticket."""
     rng = np.random.default_rng(60 + max_ctas)
     pool_rows, R, M, hot_size = 4000, 5, 257, 300
     region = hot_size + 1
@@ -234,11 +234,10 @@ def test_swap_in_fp8ds_matches_oracle(max_ctas, staged):
     hot = torch.from_numpy(hot_np.view(np.int16).copy()).view(torch.bfloat16).cuda()
     dgi = cuda(dgi0)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    staging = torch.empty(R * M * RB, dtype=torch.uint8, device="cuda") if staged else None
-    ticket = torch.zeros(2, dtype=torch.int32, device="cuda") if staged else None
+    ticket = torch.zeros(2, dtype=torch.int32, device="cuda") if claim else None
     hs.swap_in_fp8ds(hs.host_device_pointer(pool), pool_rows, RB, hot, cuda(src), cuda(dst),
                      cuda(cnt), dgi=dgi, hot_size=hot_size, region_stride=region,
-                     staging=staging, max_ctas=max_ctas, ticket=ticket, status=status)
+                     max_ctas=max_ctas, ticket=ticket, status=status)
     torch.cuda.synchronize()
     exp = hot_np.copy()
     dgi_exp = dgi0.copy()
