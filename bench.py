@@ -611,6 +611,71 @@ def bench_full_fp8(args, flush):
     return out
 
 
+def bench_lookup_swap_in(reps=20, rows=64, cap=2048, hot=4096, fresh=24, pool_rows=1 << 18):
+    """Small-miss step (fresh ids per request over a warm hot buffer): S2 and
+    S3 as one kernel (hs_hot_lookup_swap_in) against S2 followed by the
+    SwapIn (24 SMs, ticket-claimed groups, as in the step, and every SM).
+    Each repetition starts from the same state (restored outside the events)."""
+    rng = np.random.default_rng(17)
+    rb = ROW_BYTES
+    pool = inputs.pinned_empty((pool_rows, rb), torch.uint8)
+    pool.copy_(torch.randint(0, 256, (pool_rows, rb), dtype=torch.uint8))
+    inputs.host_read_pass(pool)
+    pdev = hs.host_device_pointer(pool)
+    region = hot + 1
+    ghot = torch.zeros(rows * region, rb, dtype=torch.uint8, device="cuda")
+    dgi = torch.empty(rows, hot, dtype=torch.int32, device="cuda")
+    lru = torch.empty(rows, hot, dtype=torch.int16, device="cuda")
+    hs.hot_state_reset(dgi, lru)
+    stats = torch.zeros(2, dtype=torch.int64, device="cuda")
+    slot0 = np.stack([rng.choice(pool_rows, cap, replace=False) for _ in range(rows)])
+    newest = torch.full((rows,), pool_rows + 5, dtype=torch.int32, device="cuda")
+    out = hs.hot_lookup_assign(torch.from_numpy(slot0.astype(np.int32)).cuda(), None, newest,
+                               dgi, lru, region, stats, with_split_lists=True,
+                               swap=(pdev, pool_rows, ghot, rb))
+    slot1 = slot0.copy()
+    for r in range(rows):
+        slot1[r, rng.choice(cap, fresh, replace=False)] = rng.choice(pool_rows, fresh)
+    slot1 = torch.from_numpy(slot1.astype(np.int32)).cuda()
+    torch.cuda.synchronize()
+    snap = (dgi.clone(), lru.clone())
+    ticket = torch.zeros(2, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(kind):
+        tt = []
+        for i in range(reps + 3):
+            dgi.copy_(snap[0])
+            lru.copy_(snap[1])
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record()
+            if kind == "fused":
+                hs.hot_lookup_assign(slot1, None, newest, dgi, lru, region, stats, out=out,
+                                     swap=(pdev, pool_rows, ghot, rb))
+            else:
+                hs.hot_lookup_assign(slot1, None, newest, dgi, lru, region, stats, out=out)
+                hs.swap_in(pdev, pool_rows, ghot, rb, out[2], out[3], out[4], dgi=dgi,
+                           hot_size=hot, region_stride=region, max_ctas=kind, ticket=ticket,
+                           status=status)
+            b.record()
+            b.synchronize()
+            if i >= 3:
+                tt.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(tt)
+
+    t_f = run("fused")
+    t_24 = run(24)
+    t_all = run(0)
+    misses = int(out[4].sum().item())
+    assert int(status.item()) == 0
+    del pool
+    return {"workload": f"S2+S3 on a small-miss step: {rows} requests, cap {cap}, hot {hot}, "
+                        f"{fresh} fresh ids per request, 1152-byte rows",
+            "misses": misses, "fused_us": t_f, "lookup_then_swap_in_24sm_us": t_24,
+            "lookup_then_swap_in_all_sm_us": t_all}
+
+
 def bench_gqa(hbm_peak, flush, reps=20):
     cfg = inputs.gqa_union()
     R, G, d = cfg["num_reqs"], cfg["kv_heads"], cfg["d"]
@@ -867,6 +932,8 @@ def main():
         extras["hicache"] = bench_hicache()
         torch.cuda.empty_cache()
         extras["full_hisparse_fp8"] = bench_full_fp8(args, flush)
+        torch.cuda.empty_cache()
+        extras["lookup_swap_in_fused"] = bench_lookup_swap_in()
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

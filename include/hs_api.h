@@ -147,6 +147,28 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
                          int32_t* hit_idx, int32_t* miss_rows, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * S2 + S3  hs_hot_lookup_swap_in -- [HS] hisparse_swap_in_kernel as one
+ * kernel: Phase 1 .. 4 exactly as hs_hot_lookup_assign (same arguments and
+ * outputs), then Phase 5 in the same CTA: each miss row host_pool[miss_src]
+ * is copied to hot[miss_dst] (a source outside [0, host_rows) zeroes the hot
+ * row and revokes its slot, dgi = -1, as in hs_swap_in).  One CTA per
+ * request copies that request's misses, so this suits steps with few misses
+ * per request; with many, hs_hot_lookup_assign followed by hs_swap_in
+ * spreads the copy over many SMs.
+ * host_pool   device-visible pointer to the pinned pool, host_rows rows of
+ *             row_bytes (16-byte aligned).
+ * hot         device hot buffer, rows of row_bytes (16-byte aligned).
+ * row_bytes   multiple of 16, at most 2048 (HS_ERR_CAPACITY above).
+ * ------------------------------------------------------------------------- */
+int hs_hot_lookup_swap_in(const int32_t* slot, const int32_t* count, int32_t rows, int32_t cap,
+                          int32_t num_real_rows, const int32_t* newest_slot, int32_t* dgi,
+                          int16_t* lru, int32_t hot_size, int64_t region_stride,
+                          int32_t* hot_idx, uint8_t* miss_mask, int32_t* miss_src,
+                          int64_t* miss_dst, int32_t* miss_count, int64_t* stats, int32_t* err,
+                          int32_t* hit_idx, int32_t* miss_rows, const void* host_pool,
+                          int64_t host_rows, void* hot, int64_t row_bytes, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * S3  hs_swap_in -- [HS] Phase 5 (copy each miss row host -> hot; a source
  * outside [0, host_rows) zeroes the hot row and revokes its slot, dgi = -1),
  * [HC] Modifications (copies staged through a shared-memory ring; one TMA

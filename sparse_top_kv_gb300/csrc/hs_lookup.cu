@@ -19,6 +19,14 @@
 // coalesced pass at the end (hits land at random entries: storing them from
 // the walk would cost one L1 wavefront per hit).  The output is bit-
 // identical to the sequential definition for every thread schedule.
+//
+// hs_hot_lookup_swap_in is the walkthrough's single kernel (lookup, LRU,
+// eviction and the row loads of Phase 5 in one CTA per request): after the
+// lookup the same CTA copies its request's misses from the pinned pool into
+// their hot rows, each warp two rows at a time with 16-byte loads.  It saves
+// the SwapIn launch and its hand-off for steps with few misses; with many
+// misses the separate SwapIn, which spreads one request's rows over many SMs
+// and stages them through shared memory, is the faster copy.
 #include "hs_common.cuh"
 
 namespace {
@@ -48,7 +56,15 @@ struct LookupArgs {
     int32_t hash_log2;
     int32_t* hit_idx;    // optional: hot_idx with the misses set to -1
     int32_t* miss_rows;  // optional: int32 copy of miss_dst
+    // Fused SwapIn (hot != nullptr): rows of row_bytes from host_pool.
+    const uint8_t* host_pool;
+    int64_t host_rows;
+    uint8_t* hot;
+    int64_t row_bytes;
 };
+
+constexpr int kCopyVecs = 4;   // 16-byte vectors per lane and row: rows up to 2048 B
+constexpr int kCopyRows = 2;   // rows a warp moves per round
 
 __device__ __forceinline__ uint32_t hash_of(int32_t g, int log2n) {
     return (uint32_t(g) * 2654435761u) >> (32 - log2n);
@@ -89,6 +105,7 @@ __device__ __forceinline__ int insert_key(int32_t* keys, int32_t g, int log2n) {
     return -1;  // unreachable: the table holds at least 4x the keys
 }
 
+template <bool kSwap>
 __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int scan_scratch[33];
@@ -308,6 +325,48 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
                   static_cast<unsigned long long>(M));
         a.err[row] = s_dup;
     }
+    if (!kSwap) return;
+
+    // Phase 5 (fused): the M misses host -> hot.  The miss lists and dgi
+    // were written to global memory by this CTA above.
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    const int nv = int(a.row_bytes >> 4);
+    for (int m0 = warp * kCopyRows; m0 < M; m0 += kCopyRows * (kThreads / 32)) {
+        uint4 buf[kCopyRows][kCopyVecs];
+        int64_t dst[kCopyRows];
+        bool has_src[kCopyRows];
+#pragma unroll
+        for (int u = 0; u < kCopyRows; ++u) {
+            const int mi = m0 + u;
+            dst[u] = mi < M ? mdst[mi] : -1;
+            const int32_t g = mi < M ? msrc[mi] : -1;
+            has_src[u] = dst[u] >= 0 && g >= 0 && int64_t(g) < a.host_rows;
+            if (has_src[u]) {
+                const uint4* src = reinterpret_cast<const uint4*>(a.host_pool + int64_t(g) * a.row_bytes);
+#pragma unroll
+                for (int k = 0; k < kCopyVecs; ++k) {
+                    const int v = lane + 32 * k;
+                    if (v < nv) buf[u][k] = __ldg(src + v);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyRows; ++u) {
+            if (dst[u] < 0) continue;
+            uint4* d = reinterpret_cast<uint4*>(a.hot + dst[u] * a.row_bytes);
+#pragma unroll
+            for (int k = 0; k < kCopyVecs; ++k) {
+                const int v = lane + 32 * k;
+                if (v < nv) d[v] = has_src[u] ? buf[u][k] : make_uint4(0, 0, 0, 0);
+            }
+            // No source row: the hot row is zeroed above and its slot revoked.
+            if (!has_src[u] && lane == 0) {
+                const int64_t sl = dst[u] - hot_base;
+                if (sl >= 0 && sl < hot_size) dgi[sl] = -1;
+            }
+        }
+    }
 }
 
 __global__ void reset_kernel(int32_t* dgi, int16_t* lru, int32_t hot_size) {
@@ -330,6 +389,27 @@ extern "C" int hs_hot_state_reset(int32_t* dgi, int16_t* lru, int32_t rows, int3
     return hs_host::launch_status();
 }
 
+namespace {
+template <bool kSwap>
+int lookup_launch(LookupArgs a, int32_t rows, int32_t cap, int32_t hot_size, hs_stream_t stream) {
+    // Hash of load factor <= 1/4, or <= 1/2 when the larger table does not fit.
+    const auto smem_for = [&](int l2) {
+        return size_t(8) * (size_t(1) << l2) + size_t(9) * cap + size_t(10) * hot_size;
+    };
+    int log2n = 6;
+    while ((1 << log2n) < 4 * cap) ++log2n;
+    if (smem_for(log2n) > size_t(kMaxSmem) && log2n > 6) --log2n;
+    const size_t smem = smem_for(log2n);
+    if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
+    static int smem_set[64] = {};
+    const int rc = hs_host::ensure_dynamic_smem(
+        reinterpret_cast<const void*>(lookup_kernel<kSwap>), smem, smem_set);
+    if (rc != HS_OK) return rc;
+    a.hash_log2 = log2n;
+    return hs_host::launch_pdl(lookup_kernel<kSwap>, dim3(rows), dim3(kThreads), smem, stream, a);
+}
+}  // namespace
+
 extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows,
                                     int32_t cap, int32_t num_real_rows,
                                     const int32_t* newest_slot, int32_t* dgi, int16_t* lru,
@@ -347,22 +427,42 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
         (cap > 0 && (hot_idx == nullptr || miss_src == nullptr || miss_dst == nullptr)) ||
         miss_count == nullptr || stats == nullptr || err == nullptr)
         return HS_ERR_INVALID_ARG;
-    // Hash of load factor <= 1/4, or <= 1/2 when the larger table does not fit.
-    const auto smem_for = [&](int l2) {
-        return size_t(8) * (size_t(1) << l2) + size_t(9) * cap + size_t(10) * hot_size;
-    };
-    int log2n = 6;
-    while ((1 << log2n) < 4 * cap) ++log2n;
-    if (smem_for(log2n) > size_t(kMaxSmem) && log2n > 6) --log2n;
-    const size_t smem = smem_for(log2n);
-    if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
-    static int smem_set[64] = {};
-    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(lookup_kernel),
-                                                smem, smem_set);
-    if (rc != HS_OK) return rc;
     LookupArgs a{slot,     count,    rows,     cap,        num_real_rows, newest_slot,
                  dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
-                 miss_src, miss_dst, miss_count, stats,    err,           log2n,
-                 hit_idx,  miss_rows};
-    return hs_host::launch_pdl(lookup_kernel, dim3(rows), dim3(kThreads), smem, stream, a);
+                 miss_src, miss_dst, miss_count, stats,    err,           0,
+                 hit_idx,  miss_rows, nullptr, 0, nullptr, 0};
+    return lookup_launch<false>(a, rows, cap, hot_size, stream);
+}
+
+extern "C" int hs_hot_lookup_swap_in(const int32_t* slot, const int32_t* count, int32_t rows,
+                                     int32_t cap, int32_t num_real_rows,
+                                     const int32_t* newest_slot, int32_t* dgi, int16_t* lru,
+                                     int32_t hot_size, int64_t region_stride, int32_t* hot_idx,
+                                     uint8_t* miss_mask, int32_t* miss_src, int64_t* miss_dst,
+                                     int32_t* miss_count, int64_t* stats, int32_t* err,
+                                     int32_t* hit_idx, int32_t* miss_rows, const void* host_pool,
+                                     int64_t host_rows, void* hot, int64_t row_bytes,
+                                     hs_stream_t stream) {
+    if (rows < 0 || cap < 0 || hot_size <= 0 || hot_size > 32767 || num_real_rows < 0 ||
+        host_rows < 0 || row_bytes <= 0)
+        return HS_ERR_INVALID_ARG;
+    if (row_bytes % 16 != 0) return HS_ERR_MISALIGNED;
+    if (row_bytes > 16 * 32 * kCopyVecs) return HS_ERR_CAPACITY;
+    if (region_stride < int64_t(hot_size) + 1) return HS_ERR_INVALID_ARG;
+    if (int64_t(rows) * region_stride > INT32_MAX) return HS_ERR_INVALID_ARG;
+    if (cap > hot_size) return HS_ERR_CAPACITY;
+    if (rows == 0) return HS_OK;
+    if ((cap > 0 && slot == nullptr) || dgi == nullptr || lru == nullptr ||
+        (cap > 0 && (hot_idx == nullptr || miss_src == nullptr || miss_dst == nullptr)) ||
+        miss_count == nullptr || stats == nullptr || err == nullptr || host_pool == nullptr ||
+        hot == nullptr)
+        return HS_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(host_pool) | reinterpret_cast<uintptr_t>(hot)) & 15u) != 0)
+        return HS_ERR_MISALIGNED;
+    LookupArgs a{slot,     count,    rows,     cap,        num_real_rows, newest_slot,
+                 dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
+                 miss_src, miss_dst, miss_count, stats,    err,           0,
+                 hit_idx,  miss_rows, static_cast<const uint8_t*>(host_pool), host_rows,
+                 static_cast<uint8_t*>(hot), row_bytes};
+    return lookup_launch<true>(a, rows, cap, hot_size, stream);
 }

@@ -42,6 +42,8 @@ _SIGS = {
                            _I64, _I32, _I32, _P, _P], ctypes.c_int),
     "hs_swap_in": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _P, _I32, _I64, _I32, _P, _P, _P],
                    ctypes.c_int),
+    "hs_hot_lookup_swap_in": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
+                               _P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P], ctypes.c_int),
     "hs_backup": ([_P, _P, _P, _P, _I32, _I64, _I64, _P, _P], ctypes.c_int),
     "hs_sparse_decode_workspace_bytes": ([_I32, _I32, _I32, _I32, _I32, _I32], _I64),
     "hs_sparse_decode": ([_P, _P, _P, _I64, _I64, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32,
@@ -173,10 +175,12 @@ def hot_state_reset(dgi, lru, stream=None):
 
 def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, *,
                       num_real_rows=None, out=None, with_mask=True, with_split_lists=False,
-                      stream=None):
+                      swap=None, stream=None):
     """S2.  dgi/lru are updated in place; stats int64 [2] accumulates.
     Returns (hot_idx, miss_mask, miss_src, miss_dst, miss_count, err) and, with
-    with_split_lists (or an 8-tuple `out`), also (hit_idx, miss_rows)."""
+    with_split_lists (or an 8-tuple `out`), also (hit_idx, miss_rows).
+    swap=(host_pool_dev, host_rows, hot, row_bytes): the same kernel also
+    copies the misses into the hot rows (hs_hot_lookup_swap_in)."""
     _check(slot, torch.int32, "slot")
     _check(count, torch.int32, "count")
     _check(newest_slot, torch.int32, "newest_slot")
@@ -199,10 +203,18 @@ def hot_lookup_assign(slot, count, newest_slot, dgi, lru, region_stride, stats, 
     hot_idx, miss_mask, miss_src, miss_dst, miss_count, err = out[:6]
     hit_idx, miss_rows = (out[6], out[7]) if len(out) == 8 else (None, None)
     nrr = rows if num_real_rows is None else num_real_rows
-    _call("hs_hot_lookup_assign", _ptr(slot), _ptr(count), rows, cap, nrr, _ptr(newest_slot),
-          _ptr(dgi), _ptr(lru), hot_size, region_stride, _ptr(hot_idx), _ptr(miss_mask),
-          _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), _ptr(stats), _ptr(err),
-          _ptr(hit_idx), _ptr(miss_rows), _stream(stream))
+    if swap is None:
+        _call("hs_hot_lookup_assign", _ptr(slot), _ptr(count), rows, cap, nrr,
+              _ptr(newest_slot), _ptr(dgi), _ptr(lru), hot_size, region_stride, _ptr(hot_idx),
+              _ptr(miss_mask), _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), _ptr(stats),
+              _ptr(err), _ptr(hit_idx), _ptr(miss_rows), _stream(stream))
+    else:
+        host_pool_dev, host_rows, hot, row_bytes = swap
+        _call("hs_hot_lookup_swap_in", _ptr(slot), _ptr(count), rows, cap, nrr,
+              _ptr(newest_slot), _ptr(dgi), _ptr(lru), hot_size, region_stride, _ptr(hot_idx),
+              _ptr(miss_mask), _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), _ptr(stats),
+              _ptr(err), _ptr(hit_idx), _ptr(miss_rows), ctypes.c_void_p(host_pool_dev),
+              host_rows, _ptr(hot), row_bytes, _stream(stream))
     return out
 
 
