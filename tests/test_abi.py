@@ -49,6 +49,16 @@ def test_host_side_argument_checks():
     assert L.hs_hot_lookup_assign(P, P, 1, 4, 1, P, P, P, 8, 8, P, P, P, P, P, P, P, P, P,
                                   P) == 1
     assert L.hs_hot_state_reset(P, P, 1, 40000, P) == 1
+    # Lookup + copy in one kernel: rows not a multiple of 16, rows over 2048 B.
+    assert L.hs_hot_lookup_swap_in(P, P, 1, 4, 1, P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P,
+                                   100, P, 1000, P) == 2
+    assert L.hs_hot_lookup_swap_in(P, P, 1, 4, 1, P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P,
+                                   100, P, 2064, P) == 3
+    assert L.hs_hot_lookup_swap_in(P, P, 1, 4, 1, P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P,
+                                   100, P, 1152, P) == 1
+    # fp8 SwapIn: short rows, misaligned stride.
+    assert L.hs_swap_in_fp8ds(P, 10, 640, P, 10, P, P, P, 1, 1, P, 0, 0, 0, P, P, P) == 1
+    assert L.hs_swap_in_fp8ds(P, 10, 664, P, 10, P, P, P, 1, 1, P, 0, 0, 0, P, P, P) == 2
     # Rows not a multiple of 16 bytes.
     assert L.hs_swap_in(P, 10, P, 100, P, P, P, 1, 1, P, 0, 0, 0, P, P, P) == 2
     assert L.hs_swap_in(P, 10, P, 96, P, P, P, 1, 1, P, 0, 0, -1, P, P, P) == 1
