@@ -35,7 +35,7 @@ FP8DS_ROW_BYTES = 656
 # DRAM bytes (read + write) per launch from the ncu capture summarised in
 # profiles/step_kernels_full_hisparse.md (set to None when a kernel changes
 # after the capture).
-NCU_TRAFFIC = {"attention": 131952128 + 19910912, "swap_in": 273408 + 9880832}
+NCU_TRAFFIC = {"attention": 131909632 + 20212736, "swap_in": 277760 + 9677312}
 
 
 def load_peaks():
