@@ -611,7 +611,8 @@ def bench_full_fp8(args, flush):
     return out
 
 
-def bench_lookup_swap_in(reps=20, rows=64, cap=2048, hot=4096, fresh=24, pool_rows=1 << 18):
+def bench_lookup_swap_in(reps=20, rows=64, cap=2048, hot=4096, fresh=24, pool_rows=1 << 18,
+                         profile_last=False):
     """Small-miss step (fresh ids per request over a warm hot buffer): S2 and
     S3 as one kernel (hs_hot_lookup_swap_in) against S2 followed by the
     SwapIn (24 SMs, ticket-claimed groups, as in the step, and every SM).
@@ -648,6 +649,8 @@ def bench_lookup_swap_in(reps=20, rows=64, cap=2048, hot=4096, fresh=24, pool_ro
             dgi.copy_(snap[0])
             lru.copy_(snap[1])
             torch.cuda.synchronize()
+            if profile_last and kind == "fused" and i == reps + 2:
+                torch.cuda.profiler.start()
             a, b = ev(), ev()
             a.record()
             if kind == "fused":
@@ -660,6 +663,8 @@ def bench_lookup_swap_in(reps=20, rows=64, cap=2048, hot=4096, fresh=24, pool_ro
                            status=status)
             b.record()
             b.synchronize()
+            if profile_last and kind == "fused" and i == reps + 2:
+                torch.cuda.profiler.stop()
             if i >= 3:
                 tt.append(a.elapsed_time(b) * 1e3)
         return statistics.median(tt)
@@ -744,9 +749,36 @@ def profile_run(workload):
     it a few times, then run it once more between cudaProfilerStart/Stop.
     Prints nothing; times nothing."""
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    if workload == "full_hisparse":
+    if workload == "lookup_swap_in":
+        # The small-miss step of bench_lookup_swap_in through the fused kernel.
+        torch.cuda.profiler.stop()
+        r = bench_lookup_swap_in(reps=1, profile_last=True)
+        assert r["misses"] > 0
+        return
+    if workload == "mla_decode_fp8":
+        cfg = inputs.mla_decode_fp8()
+        R = cfg["num_reqs"]
+        row_req = torch.arange(R, dtype=torch.int32, device="cuda")
+        seq = torch.full((R,), cfg["ctx"], dtype=torch.int32, device="cuda")
+        out1 = hs.normalize_indices(torch.from_numpy(cfg["cand"]).cuda(), row_req, seq,
+                                    torch.from_numpy(cfg["block_table"]).cuda(), 64,
+                                    num_pages=cfg["num_pages"])
+        tok, slot, count, err = out1
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for i in range(4):
+            flush_l2(flush)
+            torch.cuda.synchronize()
+            if i == 3:
+                torch.cuda.profiler.start()
+            hs.sparse_decode_fp8ds(cfg["q"], cfg["cache8"], slot.view(R, 1, -1), count.view(R, 1),
+                                   cfg["scale"], status=status)
+            torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        assert status.item() == 0
+        return
+    if workload in ("full_hisparse", "full_hisparse_fp8"):
         S = 6
-        cfg = setup_full(S, 0)
+        cfg = setup_full(S, 0, "fp8ds" if workload == "full_hisparse_fp8" else "bf16")
         dec = make_decoder(cfg)
         dec.warm_pool()
         di = device_inputs(cfg, dec)
@@ -864,7 +896,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--profile", default=None,
-                    choices=["full_hisparse", "mla_decode", "gqa_union"],
+                    choices=["full_hisparse", "full_hisparse_fp8", "mla_decode", "mla_decode_fp8",
+                             "gqa_union", "lookup_swap_in"],
                     help="run one workload once inside cudaProfilerStart/Stop and exit "
                          "(for ncu --profile-from-start off); prints no JSON")
     args = ap.parse_args()

@@ -322,7 +322,9 @@ int launch_xfer(XferArgs a, int64_t max_items_rows, int max_ctas, hs_stream_t st
     if (rc != HS_OK) return rc;
     if (a.dst_row_bytes == 0) a.dst_row_bytes = a.row_bytes;
     a.group = int32_t(hs::max64(1, hs::min64(kMaxGroup, int64_t(kStageBytes) / a.row_bytes)));
-    const int64_t groups = (max_items_rows + a.group - 1) / a.group;
+    // A group never spans two lists: at most ceil(list_stride / group) per list.
+    const int64_t groups = hs::min64(int64_t(a.nlists) * ((a.list_stride + a.group - 1) / a.group),
+                                     max_items_rows);
     // One CTA (192 KB of stages) per SM.
     const int64_t budget = max_ctas > 0 ? max_ctas : int64_t(hs_host::num_sms());
     const int64_t grid = hs::max64(1, hs::min64((groups + kWarps - 1) / kWarps, budget));
