@@ -470,6 +470,20 @@ int hs_sparse_decode_fp8ds(const void* q, const void* kv8, int64_t row_bytes,
                            float* lse, void* workspace, int64_t workspace_bytes_given,
                            int32_t* status, hs_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * hs_wait_selftest -- no counterpart on the pages: a test of the bounded
+ * wait that every mbarrier wait of this library goes through (a wait that
+ * cannot complete reports an error instead of hanging).  One CTA waits on an
+ * mbarrier:  mode 0: nothing arrives, the wait gives up after timeout_ns;
+ * mode 1: the barrier completes, the wait returns at once;  mode 2: nothing
+ * arrives and another warp raises the CTA's abort flag after about 20 us,
+ * so the wait gives up early.  A wait that gives up stores HS_ERR_TIMEOUT in
+ * *status (device int32); *elapsed_ns (device int64) receives the wait's
+ * wall time.  The context stays usable afterwards.
+ * ------------------------------------------------------------------------- */
+int hs_wait_selftest(int32_t mode, uint64_t timeout_ns, int32_t* status, int64_t* elapsed_ns,
+                     hs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,6 +27,51 @@ extern "C" int hs_host_device_pointer(const void* host_ptr, void** dev_ptr) {
     return HS_OK;
 }
 
+// Self-test of the bounded wait every kernel of the library goes through
+// (hs::mbar_wait_bounded): one CTA, one mbarrier that expects one arrival.
+//  mode 0: nothing arrives -> the wait gives up after timeout_ns;
+//  mode 1: thread 0 arrives first -> the wait completes;
+//  mode 2: nothing arrives, a second warp raises the CTA's abort flag after
+//          ~20 us -> the wait gives up early, as a role does when another
+//          role of its CTA failed.
+// A wait that gives up stores HS_ERR_TIMEOUT; elapsed_ns receives the wait's
+// wall time.  Nothing else is in flight, so giving up leaves no copy or
+// tensor-memory operation behind.
+namespace {
+__global__ void wait_selftest_kernel(int32_t mode, uint64_t timeout_ns, int32_t* status,
+                                     int64_t* elapsed_ns) {
+    __shared__ uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        hs::mbar_init(&bar, 1);
+        abort_flag = 0;
+        hs::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (mode == 1) hs::mbar_arrive(&bar);
+        const uint64_t t0 = hs::global_timer_ns();
+        const bool ok = hs::mbar_wait_bounded(&bar, 0, timeout_ns, mode == 2 ? &abort_flag : nullptr);
+        *elapsed_ns = int64_t(hs::global_timer_ns() - t0);
+        if (!ok) hs::set_status(status, HS_ERR_TIMEOUT);
+    } else if (threadIdx.x == 32 && mode == 2) {
+        const uint64_t t0 = hs::global_timer_ns();
+        while (hs::global_timer_ns() - t0 < 20000) {
+        }
+        abort_flag = 1;
+    }
+}
+}  // namespace
+
+extern "C" int hs_wait_selftest(int32_t mode, uint64_t timeout_ns, int32_t* status,
+                                int64_t* elapsed_ns, hs_stream_t stream) {
+    if (mode < 0 || mode > 2 || status == nullptr || elapsed_ns == nullptr)
+        return HS_ERR_INVALID_ARG;
+    wait_selftest_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(mode, timeout_ns,
+                                                                                status, elapsed_ns);
+    return hs_host::launch_status();
+}
+
 namespace hs_host {
 
 int num_sms() {

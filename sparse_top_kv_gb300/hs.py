@@ -32,6 +32,7 @@ _F32 = ctypes.c_float
 
 _SIGS = {
     "hs_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "hs_wait_selftest": ([_I32, ctypes.c_uint64, _P, _P, _P], ctypes.c_int),
     "hs_host_device_pointer": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
     "hs_normalize_indices": ([_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _I32, _P, _I32, _I32,
                               _I32, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -125,6 +126,15 @@ def _check(t, dtype, name, cuda=True):
         raise ValueError(f"{name}: must be contiguous")
     if cuda and not t.is_cuda and not t.is_pinned():
         raise ValueError(f"{name}: must be a CUDA tensor or pinned host memory")
+
+
+def wait_selftest(mode, timeout_ns, *, stream=None):
+    """Bounded-wait self-test (hs_wait_selftest); returns (status, elapsed_ns)."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _call("hs_wait_selftest", mode, timeout_ns, _ptr(status), _ptr(elapsed), _stream(stream))
+    torch.cuda.synchronize()
+    return int(status.item()), int(elapsed.item())
 
 
 def status_string(code):

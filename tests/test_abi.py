@@ -33,6 +33,10 @@ def test_status_strings():
     assert hs.status_string(0) == "HS_OK"
     assert hs.status_string(5) == "HS_ERR_TIMEOUT"
     assert hs.status_string(12345) == "HS_ERR_UNKNOWN"
+    # The wait self-test checks its mode and outputs before launching.
+    L = hs.lib()
+    assert L.hs_wait_selftest(3, 1000, None, None, None) == 1
+    assert L.hs_wait_selftest(0, 1000, None, None, None) == 1
 
 
 def test_host_side_argument_checks():
