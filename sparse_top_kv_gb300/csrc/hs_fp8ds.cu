@@ -10,13 +10,12 @@
 // before QK^T and PV).
 //
 // GB300 design.  The attention runs in two launches:
-//  * fp8ds_gather_kernel: one warp per selected row; lane i loads the codes
-//    of columns 8 i .. 8 i + 7 and 256 + 8 i .. 263 + 8 i (two 8-byte
-//    loads), their group scales, lanes 0-7 the RoPE bytes; the codes go
-//    through the hardware e4m3x2 -> f16x2 conversion, fp32 scaling and bf16
-//    rounding, and the warp writes the 1152-byte bf16 row into a per-request
-//    scratch [rows, cap, 576] with fully coalesced stores.  Each warp keeps
-//    four rows in flight.
+//  * fp8ds_gather_kernel: a warp reads 32 entries' ids at once and moves
+//    their rows four at a time; lane i loads the 16 codes of columns
+//    16 i .. 16 i + 15 (one 16-byte load) and their group scale, lanes 0-7
+//    the RoPE bytes; the codes go through the hardware e4m3x2 -> f16x2
+//    conversion, fp32 scaling and bf16 rounding, and the warp writes the
+//    1152-byte bf16 row into a per-request scratch [rows, cap, 576].
 //  * the MLA attention (hs_attention_mla.cu on tensor cores for head counts
 //    that are multiples of 16) over the scratch rows of each request (row
 //    ids r * cap + j).
@@ -34,7 +33,7 @@
 namespace {
 
 constexpr int kFp8RowBytes = 656;
-constexpr int kRowsPerWarp = 4;
+constexpr int kBatch = 4;  // rows a warp moves with one round of loads
 constexpr int kThreads = 256;
 
 struct GatherArgs {
@@ -50,10 +49,13 @@ struct GatherArgs {
     int32_t* status;
 };
 
-// Lane i of a warp owns latent columns [8 i, 8 i + 8) and [256 + 8 i, 264 + 8 i)
-// (scale groups i / 16 and 2 + i / 16): each of its two 8-byte code loads and
-// each of its two 16-byte stores is one fully coalesced 256-byte / 512-byte
-// warp access.  Lanes 0-7 also move the 128 RoPE bytes.
+// A warp takes 32 consecutive entries at a time: lane l reads entry l's
+// count and id (one coalesced load each), then the warp moves the entries
+// that have a row in batches of kBatch rows, all loads of a batch in flight
+// together (one memory latency per batch instead of three dependent ones per
+// entry).  Within a row, lane l holds the 16 codes of latent columns
+// 16 l .. 16 l + 15 (one 16-byte load; scale group l / 8) and writes their
+// 32 bf16 bytes; lanes 0-7 also move the 128 RoPE bytes.
 __global__ void __launch_bounds__(kThreads, 3) fp8ds_gather_kernel(const GatherArgs a) {
     hs::pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -61,49 +63,47 @@ __global__ void __launch_bounds__(kThreads, 3) fp8ds_gather_kernel(const GatherA
     const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
     const int64_t total = int64_t(a.rows) * a.cap;
     bool bad = false;
-    for (int64_t base = warp0 * kRowsPerWarp; base < total; base += nwarps * kRowsPerWarp) {
-        uint2 lo[kRowsPerWarp], hi[kRowsPerWarp];
-        uint4 rope[kRowsPerWarp];
-        float s_lo[kRowsPerWarp], s_hi[kRowsPerWarp];
-        int32_t id[kRowsPerWarp];
-        bool live[kRowsPerWarp];
-        // All loads of the warp's rows first.
-#pragma unroll
-        for (int u = 0; u < kRowsPerWarp; ++u) {
-            const int64_t f = base + u;
-            live[u] = false;
-            id[u] = -1;
-            if (f < total) {
-                const int r = int(f / a.cap), j = int(f - int64_t(r) * a.cap);
-                const int n = a.count ? min(max(__ldg(a.count + r), 0), a.cap) : a.cap;
-                if (j < n) {
-                    live[u] = true;
-                    id[u] = __ldg(a.kv_rows + f);
-                }
-            }
-            const bool v = live[u] && id[u] >= 0 && int64_t(id[u]) < a.num_kv_rows;
-            if (live[u] && int64_t(id[u]) >= a.num_kv_rows) bad = true;
-            if (!v) id[u] = -1;
-            if (id[u] >= 0) {
-                const unsigned char* row = a.kv8 + int64_t(id[u]) * a.row_bytes;
-                lo[u] = __ldg(reinterpret_cast<const uint2*>(row) + lane);
-                hi[u] = __ldg(reinterpret_cast<const uint2*>(row + 256) + lane);
-                const float* sc = reinterpret_cast<const float*>(row + 512);
-                s_lo[u] = __ldg(sc + (lane >> 4));
-                s_hi[u] = __ldg(sc + 2 + (lane >> 4));
-                if (lane < 8) rope[u] = __ldg(reinterpret_cast<const uint4*>(row + 528) + lane);
+    for (int64_t base = warp0 * 32; base < total; base += nwarps * 32) {
+        const int64_t f = base + lane;
+        bool live = false;
+        int32_t id = -1;
+        if (f < total) {
+            const int r = int(f / a.cap), j = int(f - int64_t(r) * a.cap);
+            const int n = a.count ? min(max(__ldg(a.count + r), 0), a.cap) : a.cap;
+            if (j < n) {
+                live = true;
+                id = __ldg(a.kv_rows + f);
             }
         }
+        const bool has_src = live && id >= 0 && int64_t(id) < a.num_kv_rows;
+        if (live && int64_t(id) >= a.num_kv_rows) bad = true;
+        if (live) a.out_ids[f] = has_src ? int32_t(f) : -1;
+        unsigned todo = __ballot_sync(0xffffffffu, has_src);
+        while (todo) {
+            uint4 code[kBatch], rope[kBatch];
+            float sc[kBatch];
+            int64_t dst[kBatch];
 #pragma unroll
-        for (int u = 0; u < kRowsPerWarp; ++u) {
-            const int64_t f = base + u;
-            if (!live[u]) continue;
-            if (lane == 0) a.out_ids[f] = id[u] >= 0 ? int32_t(f) : -1;
-            if (id[u] < 0) continue;
-            uint4* dst = reinterpret_cast<uint4*>(a.out + f * 576);
-            dst[lane] = hs::fp8_dequant8(lo[u], s_lo[u]);
-            dst[32 + lane] = hs::fp8_dequant8(hi[u], s_hi[u]);
-            if (lane < 8) dst[64 + lane] = rope[u];
+            for (int b = 0; b < kBatch; ++b) {
+                const int u = todo ? __ffs(todo) - 1 : -1;  // the same on every lane
+                todo &= todo - 1u;
+                const int32_t iu = __shfl_sync(0xffffffffu, id, u < 0 ? 0 : u);
+                dst[b] = u < 0 ? -1 : base + u;
+                if (u >= 0) {
+                    const unsigned char* row = a.kv8 + int64_t(iu) * a.row_bytes;
+                    code[b] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+                    sc[b] = __ldg(reinterpret_cast<const float*>(row + 512) + (lane >> 3));
+                    if (lane < 8) rope[b] = __ldg(reinterpret_cast<const uint4*>(row + 528) + lane);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (dst[b] < 0) continue;
+                uint4* o = reinterpret_cast<uint4*>(a.out + dst[b] * 576);
+                o[2 * lane] = hs::fp8_dequant8(make_uint2(code[b].x, code[b].y), sc[b]);
+                o[2 * lane + 1] = hs::fp8_dequant8(make_uint2(code[b].z, code[b].w), sc[b]);
+                if (lane < 8) o[64 + lane] = rope[b];
+            }
         }
     }
     if (bad) hs::set_status(a.status, HS_ERR_BAD_INDEX);
@@ -133,7 +133,7 @@ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 // Grid: enough warps for every entry, at most the resident CTAs of all SMs
 // (or max_ctas CTAs when given).
 int launch_gather(const GatherArgs& a, int64_t total, int32_t max_ctas, hs_stream_t stream) {
-    const int64_t warps = (total + kRowsPerWarp - 1) / kRowsPerWarp;
+    const int64_t warps = (total + 31) / 32;
     int64_t ctas = hs::min64((warps * 32 + kThreads - 1) / kThreads,
                              int64_t(hs_host::num_sms()) * gather_ctas_per_sm());
     if (max_ctas > 0) ctas = hs::min64(ctas, max_ctas);
