@@ -157,7 +157,9 @@ int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, int32_t rows
  * spreads the copy over many SMs.
  * host_pool   device-visible pointer to the pinned pool, host_rows rows of
  *             row_bytes (16-byte aligned).
- * hot         device hot buffer, rows of row_bytes (16-byte aligned).
+ * hot         device hot buffer, rows of row_bytes (16-byte aligned), at
+ *             least rows * region_stride rows (the misses' destinations are
+ *             the hot regions S2 assigns; no other row is written).
  * row_bytes   multiple of 16, at most 2048 (HS_ERR_CAPACITY above).
  * ------------------------------------------------------------------------- */
 int hs_hot_lookup_swap_in(const int32_t* slot, const int32_t* count, int32_t rows, int32_t cap,
