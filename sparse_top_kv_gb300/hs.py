@@ -355,6 +355,8 @@ def swap_in_fp8ds(host_pool_dev, host_rows, host_row_bytes, hot, miss_src, miss_
     _check(dgi, torch.int32, "dgi")
     _check(ticket, torch.int32, "ticket")
     _check(status, torch.int32, "status")
+    if ticket is not None and ticket.numel() < 2:
+        raise ValueError("ticket needs 2 int32 words")
     rows, cap = miss_src.shape
     _call("hs_swap_in_fp8ds", ctypes.c_void_p(host_pool_dev), host_rows, host_row_bytes,
           _ptr(hot), hot.shape[0], _ptr(miss_src), _ptr(miss_dst), _ptr(miss_count), rows, cap,
