@@ -32,9 +32,8 @@ from sparse_top_kv_gb300.pipeline import HiSparseDecoder  # noqa: E402
 L2_FLUSH_BYTES = 512 << 20
 ROW_BYTES = 1152
 FP8DS_ROW_BYTES = 656
-# DRAM bytes (read + write) per launch from the ncu capture summarised in
-# profiles/step_kernels_full_hisparse.md (set to None when a kernel changes
-# after the capture).
+# DRAM bytes (read + write) per launch from an ncu capture of the same
+# launches (set to None when a kernel changes after the capture).
 NCU_TRAFFIC = {"attention": 131909632 + 20212736, "swap_in": 277760 + 9677312}
 
 

@@ -367,7 +367,10 @@ int hs_sparse_decode_finish(const void* q, const void* k_base, const void* v_bas
  *   HS_NOALLOC_WORKSPACE_BYTES are rejected with HS_ERR_CAPACITY.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept for the life of the
+ *   process: after cudaDeviceReset (or any reset of the primary context)
+ *   the library's module is unloaded and the kept address is stale, so do
+ *   not call this entry point again in that process.
  * - Every call on a device shares the one array, which keeps the previous
  *   call's contents (nothing in it needs to start at zero).  Calls whose
  *   executions overlap on the GPU (e.g. on two streams) race on it: order

@@ -22,6 +22,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "hs_attention_internal.cuh"
 #include "hs_common.cuh"
@@ -990,7 +991,10 @@ extern "C" int hs_merge_states(const float* m, const float* l, const float* o, i
 // a stand-in and is never passed to a kernel.
 namespace {
 __device__ __align__(256) unsigned char g_noalloc_workspace[HS_NOALLOC_WORKSPACE_BYTES];
-void* g_noalloc_workspace_dev[64] = {};
+// Device address of the array per device, looked up once per process.  Two
+// host threads making their first call at once may both look it up; they
+// store the same value, and the atomic makes that well defined.
+std::atomic<void*> g_noalloc_workspace_dev[64];
 }  // namespace
 
 extern "C" int hs_sparse_decode_noalloc(const void* q, const void* k_base, const void* v_base,
@@ -1008,15 +1012,14 @@ extern "C" int hs_sparse_decode_noalloc(const void* q, const void* k_base, const
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
         if (dev < 0 || dev >= 64) return HS_ERR_UNSUPPORTED;
-        if (g_noalloc_workspace_dev[dev] == nullptr) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr) {
+        ws = g_noalloc_workspace_dev[dev].load(std::memory_order_acquire);
+        if (ws == nullptr) {
+            if (cudaGetSymbolAddress(&ws, g_noalloc_workspace) != cudaSuccess || ws == nullptr) {
                 cudaGetLastError();
                 return HS_ERR_CUDA;
             }
-            g_noalloc_workspace_dev[dev] = p;
+            g_noalloc_workspace_dev[dev].store(ws, std::memory_order_release);
         }
-        ws = g_noalloc_workspace_dev[dev];
     }
     return hs_sparse_decode(q, k_base, v_base, row_stride, kv_head_stride, num_kv_rows, kv_rows,
                             count, rows, cap, heads, kv_heads, d_qk, d_v, scale, out, lse, ws,

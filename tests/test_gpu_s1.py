@@ -87,3 +87,33 @@ def test_full_size_configs():
     ref = run_both(cfg5["cand"], cfg5["row_req"], np.full(16, cfg5["ctx"], np.int32),
                    cfg5["block_table"], 16, window=256, sinks=4, num_pages=cfg5["num_pages"])
     assert (ref[3][:, 3] > 0).all()  # the deliberate overlaps were counted
+
+
+@pytest.mark.parametrize("B", [16, 12])
+def test_block_table_rows_beyond_the_staged_limit(B):
+    """Block-table rows longer than the kernel stages in shared memory
+    (16384 blocks): page lookups go to global memory; power-of-two and
+    other page sizes, several bitmap windows, foreign and out-of-pool pages,
+    positions past the table."""
+    rng = np.random.default_rng(900 + B)
+    max_blocks = 20000
+    num_reqs = 2
+    num_pages = num_reqs * max_blocks + 50
+    table = rng.permutation(num_pages)[: num_reqs * max_blocks].reshape(num_reqs, max_blocks)
+    table = table.astype(np.int32)
+    table[0, 17000] = num_pages + 3   # outside the pool
+    table[1, 16384] = -1
+    owner = np.full(num_pages, -1, np.int32)
+    for q in range(num_reqs):
+        ok = (table[q] >= 0) & (table[q] < num_pages)
+        owner[table[q][ok]] = q
+    owner[table[1, 19999]] = 0        # a foreign page
+    T = max_blocks * B
+    seq = np.array([T, T - 5], np.int32)
+    edges = np.array([0, 16383 * B, 16384 * B, 16384 * B + 1, 17000 * B + 2, 19999 * B,
+                      T - 1, T, T + 3, -1])
+    cand = np.concatenate([edges, rng.integers(0, T + 10, size=4000)]).astype(np.int32)
+    cand = np.stack([cand, rng.permutation(cand)])
+    cand[:, 20:40] = cand[:, 40:60]   # repeats
+    run_both(cand, np.array([0, 1], np.int32), seq, table, B, window=3000, sinks=7,
+             owner=owner, num_pages=num_pages)
