@@ -835,10 +835,11 @@ def profile_run(workload):
 
 
 # ----------------------------------------------------------------------------
-def oracle_steps(cfg, steps, attend_rows):
-    """Time the oracle's decode step (S1-S3 + BackUp on every request, S4 on
-    `attend_rows` requests) on the host; returns per-step seconds, S4 part and
-    the S1-S3 part."""
+def oracle_steps(cfg, steps, attend_from):
+    """Run the oracle's decode step over steps 0 .. steps-1 of the workload on
+    the host from a cold state; steps >= attend_from are whole (S1-S3,
+    BackUp and S4 on every request), earlier ones only advance the state
+    (S1-S3 and BackUp: S4 changes no state).  Returns per-step seconds."""
     from oracle.pipeline import OracleHiSparse
     import oracle as _o
     _o.lib()
@@ -857,32 +858,16 @@ def oracle_steps(cfg, steps, attend_rows):
         newest = ora.newest_slots(np.full(R, T - 1, np.int32), seq)
         t0 = time.perf_counter()
         ora.step(cfg["cand"][s], seq, newest, new_u8[s].reshape(R, ROW_BYTES), q_bits[s],
-                 attend_rows=attend_rows)
+                 attend_rows=None if s >= attend_from else [])
         secs.append(time.perf_counter() - t0)
     return secs
 
 
-def cpu_baseline_full(cfg, steps, sample_rows):
-    """Bounded sample: `steps` oracle steps from a cold state; S4 on
-    `sample_rows` of the 64 requests, scaled to all 64 (S4 is per-request)."""
-    t_all = oracle_steps(cfg, steps, attend_rows=list(range(sample_rows)))
-    t_none = None
-    # Separate S4 from the rest: time the S4-free part on the same steps again.
-    est = []
-    R = cfg["num_reqs"]
-    for t in t_all:
-        est.append(t)
-    # Scale: run one more pass with no attention to isolate S1-S3 + BackUp.
-    t_nos4 = oracle_steps(cfg, steps, attend_rows=[])
-    per = []
-    for a, b in zip(t_all, t_nos4):
-        s4 = max(0.0, a - b)
-        per.append(b + s4 * R / sample_rows)
-    # Steady state: skip the cold step 0 when there is more than one.
-    steady = per[1:] if len(per) > 1 else per
-    sec = statistics.mean(steady)
-    del t_none, est
-    return sec
+def cpu_baseline_full(cfg, steps=3):
+    """Bounded sample: whole oracle steps 1 .. steps of full_hisparse after
+    its cold step 0 (which only advances the state); mean seconds per step."""
+    secs = oracle_steps(cfg, steps + 1, attend_from=1)
+    return statistics.mean(secs[1:])
 
 
 # ----------------------------------------------------------------------------
@@ -969,10 +954,11 @@ def main():
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        sec = cpu_baseline_full(full["cfg"], 3, 4)
+        sec = cpu_baseline_full(full["cfg"], 3)
         cpu = {"value": 1.0 / sec, "unit": "steps/s", "cores": 1, "kind": "oracle",
-               "sample": "oracle steps 0-2 of full_hisparse from a cold state: S1-S3 and BackUp "
-                         "on all 64 requests, S4 on 4 requests scaled x16; mean of steps 1-2"}
+               "sample": "whole oracle steps 1-3 of full_hisparse (S1-S3, BackUp and S4 on all "
+                         "64 requests) after its cold step 0, mean of the three; one host "
+                         "thread"}
     line = {
         "metric": "sparse-decode steps/s (full HiSparse step: S1 normalize, S2 LRU lookup, "
                   "S3 SwapIn+BackUp, S4 MLA decode)",
@@ -1014,21 +1000,22 @@ def main():
 
 
 def run_reference(args, rank, world):
-    """The oracle, as it stands, on the host cores: the same workload, metric
-    and unit, each step a bounded sample (S1-S3 and BackUp on all requests, S4
-    on 4 of 64 requests, scaled)."""
+    """The oracle, as it stands, on one host core: the same workload, metric
+    and unit.  The W warm-up steps advance the oracle's state (S1-S3 and
+    BackUp); each of the K timed steps is a whole step (S1-S3, BackUp and S4
+    on all 64 requests), timed with the host clock."""
     if rank != 0:
         return
     S = args.warmup + args.steps
     cfg = inputs.full_hisparse(steps=S)
-    # Both passes start from a cold oracle state over the same pool: BackUp
-    # writes the same rows in both, and step s reads only positions < T_s.
-    t_s4 = oracle_steps(cfg, S, attend_rows=[0, 1, 2, 3])
-    t_nos4 = oracle_steps(cfg, S, attend_rows=[])
-    per = [b + max(0.0, a - b) * 16 for a, b in zip(t_s4, t_nos4)]
-    timed = per[args.warmup:]
+    t_start = time.perf_counter()
+    secs = oracle_steps(cfg, S, attend_from=args.warmup)
+    wall = time.perf_counter() - t_start
+    timed = secs[args.warmup:]
     total = sum(timed)
     value = len(timed) / total
+    sample = ("every timed step whole: S1-S3, BackUp and S4 on all 64 requests; the warm-up "
+              "steps run S1-S3 and BackUp only (they advance the LRU state)")
     line = {"impl": "reference",
             "metric": "sparse-decode steps/s (full HiSparse step: S1 normalize, S2 LRU lookup, "
                       "S3 SwapIn+BackUp, S4 MLA decode)",
@@ -1038,9 +1025,9 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded)",
             "config": {"workload": "full_hisparse (as the main arm)", "global_batch": 64,
                        "seq_len": 131072, "parallelism": "single host core"},
+            "timed_s": total, "oracle_wall_s": wall,
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                             "sample": "every step: S1-S3 + BackUp on all 64 requests, S4 on 4 "
-                                       "requests scaled x16"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
