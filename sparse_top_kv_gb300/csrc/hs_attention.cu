@@ -313,18 +313,34 @@ __global__ void merge_kernel(const float* __restrict__ pm, const float* __restri
 // Host side: kernel choice and split policy.
 
 struct Plan {
-    int kind;  // 0 unsupported, 1 MLA on CUDA cores, 2 GQA d=128, 3 MLA on tcgen05
+    int kind;  // 0 unsupported, 1 MLA on CUDA cores, 2 GQA d=128, 3 MLA on tcgen05,
+               // 4 MLA with 128 heads on tcgen05 CTA pairs
     int G;     // heads per CTA
     int chunks_per_kvh;
     int splits;
     int kv_heads;
 };
 
-Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bool shared) {
+// pair_ok: the one-call decode (no caller-held partial columns) may use the
+// CTA-pair kernel for 128 heads.
+Plan make_plan(int rows, int heads, int kv_heads, int cap, int d_qk, int d_v, bool shared,
+               bool pair_ok) {
     Plan p{0, 0, 0, 1, kv_heads};
     if (rows <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads) return p;
     const int group = heads / kv_heads;
     const bool mla = d_qk == 576 && d_v == 512 && kv_heads == 1 && shared;
+    if (mla && heads == 128 && pair_ok) {
+        // One CTA pair per (row, split): every row of a 256-row pair tile is
+        // gathered once for all 128 heads; splits fill the SM pairs once.
+        p.kind = 4;
+        p.G = 128;
+        p.chunks_per_kvh = 1;
+        const int64_t pairs = hs::max64(1, hs_host::num_sms() / 2);
+        int64_t s = rows >= pairs ? 1 : pairs / rows;
+        s = hs::min64(s, hs::max64(1, (cap + 255) / 256));
+        p.splits = int(hs::max64(1, hs::min64(s, kMlaPairMaxSplits)));
+        return p;
+    }
     if (mla && mla_tc_head_group(heads) > 0) {
         // Tensor-core kernel: one CTA per SM (about 220 KB of shared memory);
         // split the candidate list so that the grid fills the SMs once.
@@ -372,8 +388,19 @@ int64_t sync_words(const Plan& p, int rows) {
     return int64_t(rows) * p.kv_heads * p.chunks_per_kvh;
 }
 
+// CTA-pair kernel: partial O, then (m, l) per CTA rank, then counters.
+int64_t pair_part_o_bytes(const Plan& p, int rows) {
+    return int64_t(rows) * 128 * p.splits * 512 * int64_t(sizeof(float));
+}
+int64_t pair_part_ml_bytes(const Plan& p, int rows) {
+    return 2 * int64_t(rows) * 128 * p.splits * 2 * int64_t(sizeof(float));
+}
+
 int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
     if (p.kind == 0 || p.splits <= 1) return 0;
+    if (p.kind == 4)
+        return pair_part_o_bytes(p, rows) + pair_part_ml_bytes(p, rows) +
+               (int64_t(rows) * 4 * 4 + 15) / 16 * 16;
     int64_t b = partial_bytes(p, rows, heads, d_v);
     if (p.kind == 3 || p.kind == 2) b += (sync_words(p, rows) * 4 + 15) / 16 * 16;
     return b;
@@ -751,7 +778,8 @@ using namespace hs_attn;
 extern "C" int64_t hs_sparse_decode_workspace_bytes(int32_t rows, int32_t heads,
                                                     int32_t kv_heads, int32_t cap,
                                                     int32_t d_qk, int32_t d_v) {
-    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, kv_heads == 1 && d_qk == 576);
+    const Plan p =
+        make_plan(rows, heads, kv_heads, cap, d_qk, d_v, kv_heads == 1 && d_qk == 576, true);
     return workspace_bytes(p, rows, heads, d_v);
 }
 
@@ -785,7 +813,7 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
         row_stride % 8 || kv_head_stride % 8)
         return HS_ERR_MISALIGNED;
     const bool shared = k_base == v_base;
-    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, shared);
+    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, shared, po == nullptr);
     if (p.kind == 0) return HS_ERR_UNSUPPORTED;
     const int64_t n = int64_t(rows) * heads;
     AttnArgs a{};
@@ -823,6 +851,35 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
     } else {
         const int64_t ws = workspace_bytes(p, rows, heads, d_v);
         if (ws > 0 && (workspace == nullptr || workspace_bytes_given < ws)) return HS_ERR_CAPACITY;
+        if (p.kind == 4) {
+            MlaArgs m{};
+            m.q = static_cast<const __nv_bfloat16*>(q);
+            m.kv = static_cast<const __nv_bfloat16*>(k_base);
+            m.row_stride = row_stride;
+            m.num_kv_rows = num_kv_rows;
+            m.kv_rows = kv_rows;
+            m.count = count;
+            m.rows = rows;
+            m.cap = cap;
+            m.heads = heads;
+            m.scale_log2 = scale * kLog2e;
+            m.out = static_cast<__nv_bfloat16*>(out);
+            m.lse = lse;
+            m.splits = p.splits;
+            m.status = status;
+            m.timeout_ns = hs::kWaitTimeoutNs;
+            if (p.splits > 1) {
+                unsigned char* w = static_cast<unsigned char*>(workspace);
+                m.part_o = reinterpret_cast<float*>(w);
+                m.part_m = reinterpret_cast<float*>(w + pair_part_o_bytes(p, rows));
+                m.sync = reinterpret_cast<int32_t*>(w + pair_part_o_bytes(p, rows) +
+                                                    pair_part_ml_bytes(p, rows));
+                if (cudaMemsetAsync(m.sync, 0, size_t(rows) * 4 * sizeof(int32_t),
+                                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                    return HS_ERR_CUDA;
+            }
+            return launch_mla_pair(m, rows * p.splits, stream);
+        }
         if (p.splits > 1) {
             float* w = static_cast<float*>(workspace);
             a.part_m = w;
@@ -938,7 +995,8 @@ extern "C" int hs_sparse_decode(const void* q, const void* k_base, const void* v
 
 extern "C" int32_t hs_sparse_decode_partial_splits(int32_t rows, int32_t heads, int32_t kv_heads,
                                                    int32_t cap, int32_t d_qk, int32_t d_v) {
-    const Plan p = make_plan(rows, heads, kv_heads, cap, d_qk, d_v, kv_heads == 1 && d_qk == 576);
+    const Plan p =
+        make_plan(rows, heads, kv_heads, cap, d_qk, d_v, kv_heads == 1 && d_qk == 576, false);
     return p.kind == 0 ? 0 : p.splits;
 }
 

@@ -39,6 +39,15 @@ struct MlaArgs {
 // Columns the last-CTA merge of the tcgen05 kernel can combine.
 constexpr int kMlaMaxMerge = 8;
 
+// Splits of one row the CTA-pair kernel (128 heads) can merge in its epilogue.
+constexpr int kMlaPairMaxSplits = 8;
+
+// CTA-pair kernel for 128 heads: grid = 2 * rows * splits CTAs (clusters of
+// two).  Workspace when splits > 1: part_o = [rows * 128, splits, 512] fp32,
+// part_m = [2, rows * 128, splits, 2] fp32 (m, l per CTA rank), sync =
+// [rows, 2, 2] int32 counters, zero on entry and left zero.
+int launch_mla_pair(const MlaArgs& a, int pairs, hs_stream_t stream);
+
 // Query heads handled by one CTA (64, 32 or 16), or 0 when heads % 16 != 0.
 int mla_tc_head_group(int heads);
 // grid = (rows * heads / hg, splits).
