@@ -210,6 +210,43 @@ def full_hisparse(steps=16, num_reqs=64, top_k=2048, heads=16, pool_on_gpu_seed=
     return cfg
 
 
+def multi_layer_hisparse(layers=4, num_reqs=64, total=32768, top_k=2048, steps=16, heads=16,
+                         page_size=64, keep_frac=0.85, zipf_s=1.1, seed=None):
+    """Several HiSparse layers that share each step's index stream (one top-k
+    row per request and step, drawn as in full_hisparse: step 0 uniform, then
+    round(keep_frac * top_k) kept and the rest Zipf(zipf_s) over recency).
+    Layer l has its own pool of N(0, 1) bf16 rows (pinned; drawn on the GPU
+    when it is large), its own queries and its own new rows, all seeded from
+    seed + 1000 l.  Returns the shared fields plus per-layer lists
+    pools, q and new_rows."""
+    seed = SEEDS["full_hisparse"] + 10 if seed is None else seed
+    pages_per_req = total // page_size
+    num_pages = num_reqs * pages_per_req
+    cfg = dict(name="multi_layer_hisparse", layers=layers, num_reqs=num_reqs, heads=heads,
+               d_qk=576, d_v=512, page_size=page_size, total_positions=total, steps=steps,
+               top_k=top_k, hot_size=2 * top_k, region_stride=2 * top_k + 1,
+               scale=1.0 / math.sqrt(576.0), seed=seed, num_pages=num_pages)
+    cfg["prefill"] = total - steps
+    cfg["block_table"] = page_table(num_reqs, pages_per_req, num_pages, seed)
+    cfg["cand"] = hisparse_index_steps(num_reqs, top_k, cfg["prefill"], steps,
+                                       keep=round(keep_frac * top_k), seed=seed, zipf_s=zipf_s)
+    cfg["newest_pos"] = np.array([[cfg["prefill"] + s] * num_reqs for s in range(steps)],
+                                 np.int32)
+    rows = num_pages * page_size
+    pools, qs, news = [], [], []
+    for l in range(layers):
+        ls = seed + 1000 * l
+        if rows * 576 * 2 > (256 << 20):
+            pools.append(fill_randn_bf16_pinned(rows, 576, ls + 100))
+        else:
+            pools.append(randn_bf16((rows, 576), ls + 100).pin_memory())
+        g = torch.Generator(device="cpu").manual_seed(ls + 200)
+        qs.append(torch.randn(steps, num_reqs, heads, 576, generator=g).to(torch.bfloat16))
+        news.append(torch.randn(steps, num_reqs, 576, generator=g).to(torch.bfloat16))
+    cfg["pools"], cfg["q"], cfg["new_rows"] = pools, qs, news
+    return cfg
+
+
 # ----------------------------------------------------------------------------
 
 def swapin(num_reqs=64, misses=4096, pool_rows=1 << 20, row_bytes=1152, seed=None):

@@ -362,3 +362,122 @@ class HiSparseDecoder:
     # with the merge in its epilogue.
     def launches_per_step(self):
         return 6
+
+
+class MultiLayerHiSparse:
+    """Several layers of HiSparse state (one HiSparseDecoder each: its own
+    pinned pool, hot buffer and LRU state) that share each step's index row,
+    overlapped layer by layer (the layerwise offload of the vLLM HiSparse
+    walkthrough's overview and of the SGLang HiCache PR's motivation).
+
+    One step: S1 once (the index row is shared); on an index stream, each
+    layer's S2 right after S1; on a copy stream, per layer and in layer
+    order, the new row's write, its BackUp and the SwapIn of that layer's
+    misses, so the host link stays busy from the first SwapIn to the last;
+    on the main stream, per layer and in layer order (a layer's query
+    depends on the previous layer's output), the attention over the rows
+    that were resident (while that layer's SwapIn copies) and then over the
+    swapped rows, merged with eq. (7), as in HiSparseDecoder.step."""
+
+    def __init__(self, decoders):
+        if not decoders:
+            raise ValueError("at least one layer")
+        d0 = decoders[0]
+        for d in decoders[1:]:
+            if (d.num_reqs, d.cap, d.page_size, d.num_pages, d.heads, d.fp8) != (
+                    d0.num_reqs, d0.cap, d0.page_size, d0.num_pages, d0.heads, d0.fp8):
+                raise ValueError("layers must share the index geometry")
+        self.layers = list(decoders)
+        dev = d0.device
+        self.index_stream = torch.cuda.Stream(device=dev)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        L = len(decoders)
+        self.ev_s1 = torch.cuda.Event()
+        self.ev_s2 = [torch.cuda.Event() for _ in range(L)]
+        self.ev_new = [torch.cuda.Event() for _ in range(L)]
+        self.ev_swap = [torch.cuda.Event() for _ in range(L)]
+
+    def step(self, cand, seq_lens, newest_slot, new_rows, qs, stream=None):
+        """cand int32 [R, top_k], seq_lens int32 [R], newest_slot int32 [R]
+        (shared by every layer); new_rows[l] and qs[l] as in
+        HiSparseDecoder.step.  Returns [(out, lse)] per layer."""
+        d0 = self.layers[0]
+        R = d0.num_reqs
+        main = stream if stream is not None else torch.cuda.current_stream(d0.device)
+        idx_s, cp_s = self.index_stream, self.copy_stream
+        tok, slot, count, err = hs.normalize_indices(
+            cand, d0.row_req, seq_lens, d0.block_table, d0.page_size, window=d0.window,
+            num_sinks=d0.num_sinks, num_pages=d0.num_pages, out=d0.s1_out, stream=main)
+        self.ev_s1.record(main)
+        idx_s.wait_event(self.ev_s1)
+        lists = []
+        for l, dec in enumerate(self.layers):
+            lists.append(hs.hot_lookup_assign(slot, count, newest_slot, dec.dgi, dec.lru,
+                                              dec.region_stride, dec.stats, out=dec.s2_out,
+                                              stream=idx_s))
+            self.ev_s2[l].record(idx_s)
+        for l, dec in enumerate(self.layers):
+            (hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr, hit_idx,
+             miss_rows) = lists[l]
+            cp_s.wait_event(self.ev_s2[l])
+            new_row = new_rows[l]
+            if dec.fp8:
+                hs.swap_in_fp8ds(hs.device_address(new_row), R, dec.row_bytes, dec.hot,
+                                 dec.new_src, dec.new_dst, dec.new_cnt, max_ctas=0,
+                                 status=dec.status, stream=cp_s)
+                hs.backup(new_row, dec.new_rows_idx, dec.host_dev, newest_slot, dec.row_bytes,
+                          dec.host_rows, status=dec.status, stream=cp_s)
+            else:
+                with torch.cuda.stream(cp_s):
+                    dec.hot.index_copy_(0, dec.reserved_rows, new_row)
+                hs.backup(dec.hot, dec.reserved_rows, dec.host_dev, newest_slot,
+                          dec.row_bytes, dec.host_rows, status=dec.status, stream=cp_s)
+            self.ev_new[l].record(cp_s)
+            if dec.fp8:
+                hs.swap_in_fp8ds(dec.host_dev, dec.host_rows, dec.row_bytes, dec.hot, miss_src,
+                                 miss_dst, miss_count, dgi=dec.dgi, hot_size=dec.hot_size,
+                                 region_stride=dec.region_stride, max_ctas=dec.swap_ctas,
+                                 ticket=dec.ticket, status=dec.status, stream=cp_s)
+            else:
+                hs.swap_in(dec.host_dev, dec.host_rows, dec.hot, dec.row_bytes, miss_src,
+                           miss_dst, miss_count, dgi=dec.dgi, hot_size=dec.hot_size,
+                           region_stride=dec.region_stride, max_ctas=dec.swap_ctas,
+                           ticket=dec.ticket, status=dec.status, stream=cp_s)
+            if not torch.cuda.is_current_stream_capturing():
+                new_row.record_stream(cp_s)
+            self.ev_swap[l].record(cp_s)
+        outs = []
+        for l, dec in enumerate(self.layers):
+            hit_idx, miss_rows, miss_count = lists[l][6], lists[l][7], lists[l][4]
+            qv = HiSparseDecoder.q_view(qs[l])
+            nkv = dec.hot.shape[0]
+            main.wait_event(self.ev_new[l])
+            hs.sparse_decode_partial(qv, dec.hot, dec.hot, dec.row_width, 0, nkv,
+                                     hit_idx.view(R, 1, dec.cap), count.view(R, 1), dec.scale,
+                                     dec.d_v, dec.part_m, dec.part_l, dec.part_o, 0,
+                                     status=dec.status, stream=main)
+            main.wait_event(self.ev_swap[l])
+            out, lse = hs.sparse_decode_finish(qv, dec.hot, dec.hot, dec.row_width, 0, nkv,
+                                               miss_rows.view(R, 1, dec.cap),
+                                               miss_count.view(R, 1), dec.scale, dec.d_v,
+                                               dec.part_m, dec.part_l, dec.part_o,
+                                               dec.parts_hit, sync=dec.sync, out=dec.out,
+                                               lse=dec.lse, status=dec.status, stream=main)
+            outs.append((out, lse))
+        return outs
+
+    def capture(self, cand, seq_lens, newest_slot, new_rows, qs):
+        """The step over these (device) input tensors as one CUDA graph, every
+        stream included; run one eager step first.  Returns the graph."""
+        g = torch.cuda.CUDAGraph()
+        cur = torch.cuda.current_stream(self.layers[0].device)
+        self.index_stream.wait_stream(cur)
+        self.copy_stream.wait_stream(cur)
+        with torch.cuda.graph(g):
+            self.step(cand, seq_lens, newest_slot, new_rows, qs)
+        return g
+
+    # Kernels of libhs per step: S1, then per layer S2, BackUp, SwapIn and
+    # the two attention passes (index_copy_ is torch's).
+    def launches_per_step(self):
+        return 1 + 5 * len(self.layers)
