@@ -269,7 +269,7 @@ def run_full(args, rank, world, flush, row_format="bf16"):
             dec.replay_packed(packed[s])
             torch.cuda.synchronize()
             e = lambda i, j: gev[i].elapsed_time(gev[j])  # noqa: E731
-            # S1, S2, SwapIn start latency, SwapIn, resident rows,
+            # S1 + S2 (one kernel), (none), SwapIn start latency, SwapIn, resident rows,
             # swapped rows + merge (+ BackUp behind it), whole step.
             stage_ms += np.array([e(0, 1), e(1, 2), e(2, 3), e(3, 4), e(2, 5),
                                   min(e(4, 6), e(5, 6)), e(0, 6)])
@@ -601,7 +601,7 @@ def bench_full_fp8(args, flush):
                        "5.50 GB, 656 B per row), bf16 hot buffer",
            "steps_per_s": K / (r["total_ms"] / 1e3), "ms_per_step": r["total_ms"] / K,
            "hit_rate": r["hit_rate"], "swap_bytes_per_step": r["swap_bytes_per_step"],
-           "stage_us": {"s1": st[0] * 1e3, "s2": st[1] * 1e3, "swap_in": st[3] * 1e3,
+           "stage_us": {"s1_s2": st[0] * 1e3, "swap_in": st[3] * 1e3,
                         "resident_rows": st[4] * 1e3, "swapped_rows_merge": st[5] * 1e3},
            "swap_in_gbs": r["swap_bytes_per_step"] / (st[3] * 1e6) if st[3] > 0 else None,
            "step_us_timed": [round(x * 1e3, 1) for x in r["step_ms"]],
@@ -1094,7 +1094,7 @@ def main():
         "step_us_timed": [round(x * 1e3, 1) for x in full["step_ms"]],
         "stage_us_note": "timed steps replay one CUDA graph per step; stage_us from "
                          + full["stage_src"],
-        "stage_us": {"s1_normalize": stage[0] * 1e3, "s2_lookup": stage[1] * 1e3,
+        "stage_us": {"s1_s2_normalize_lookup (one kernel)": stage[0] * 1e3,
                      "swap start": stage[2] * 1e3,
                      "s3_swap_in": stage[3] * 1e3,
                      "s4_resident_rows (side stream, overlaps the swap)": stage[4] * 1e3,

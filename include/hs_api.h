@@ -171,6 +171,31 @@ int hs_hot_lookup_swap_in(const int32_t* slot, const int32_t* count, int32_t row
                           int64_t host_rows, void* hot, int64_t row_bytes, hs_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * S1 + S2  hs_normalize_lookup_assign -- [PT] 1.1 eq. (1), 1.2 eq. (2), 7.3
+ * eq. (16) and [HS] hisparse_swap_in_kernel Phase 1 .. 4 in one kernel: each
+ * index row is normalised exactly as hs_normalize_indices does (same
+ * arguments and outputs: out_tok, out_slot, out_count, err_counts) and its
+ * slots are then looked up and assigned exactly as hs_hot_lookup_assign does
+ * with slot = out_slot and count = out_count (same state and outputs; row r
+ * of the index rows uses state row r, num_real_rows = rows).  One CTA per
+ * row: the row's dgi / lru are copied into shared memory while S1 runs, and
+ * S1's ascending set stays in shared memory for the lookup, so the two
+ * stages cost one launch and no round trip through global memory.  Every
+ * argument is checked as by the two calls; cap <= hot_size.
+ * ------------------------------------------------------------------------- */
+int hs_normalize_lookup_assign(const int32_t* cand, int32_t rows, int32_t n_cand, int32_t window,
+                               int32_t num_sinks, const int32_t* row_req, const int32_t* seq_lens,
+                               const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                               const int32_t* page_owner, int32_t num_reqs, int32_t num_pages,
+                               int32_t page_size, int32_t cap, int32_t* out_tok,
+                               int32_t* out_slot, int32_t* out_count, int32_t* err_counts,
+                               const int32_t* newest_slot, int32_t* dgi, int16_t* lru,
+                               int32_t hot_size, int64_t region_stride, int32_t* hot_idx,
+                               uint8_t* miss_mask, int32_t* miss_src, int64_t* miss_dst,
+                               int32_t* miss_count, int64_t* stats, int32_t* err,
+                               int32_t* hit_idx, int32_t* miss_rows, hs_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * S3  hs_swap_in -- [HS] Phase 5 (copy each miss row host -> hot; a source
  * outside [0, host_rows) zeroes the hot row and revokes its slot, dgi = -1),
  * [HC] Modifications (copies staged through a shared-memory ring; one TMA

@@ -27,7 +27,7 @@
 // the SwapIn launch and its hand-off for steps with few misses; with many
 // misses the separate SwapIn, which spreads one request's rows over many SMs
 // and stages them through shared memory, is the faster copy.
-#include "hs_common.cuh"
+#include "hs_norm_core.cuh"
 
 namespace {
 
@@ -61,6 +61,11 @@ struct LookupArgs {
     int64_t host_rows;
     uint8_t* hot;
     int64_t row_bytes;
+    // Fused S1 (kNorm): the row's candidates are normalised in the same CTA
+    // (norm.cand ...; S1's outputs to norm.out_tok/out_slot/out_count/
+    // err_counts) and `slot`/`count` above are not read.
+    hs_norm::NormArgs norm;
+    int32_t state_async;  // 1: dgi / lru rows 16-byte aligned, copied with cp.async
 };
 
 constexpr int kCopyVecs = 4;   // 16-byte vectors per lane and row: rows up to 2048 B
@@ -105,7 +110,7 @@ __device__ __forceinline__ int insert_key(int32_t* keys, int32_t g, int log2n) {
     return -1;  // unreachable: the table holds at least 4x the keys
 }
 
-template <bool kSwap>
+template <bool kSwap, bool kNorm>
 __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int scan_scratch[33];
@@ -123,6 +128,14 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     int16_t* E = s_lru + hot_size;
     int16_t* H = E + hot_size;
     uint8_t* kind = reinterpret_cast<uint8_t*>(H + hot_size);  // kNone / kHit / kMiss
+    // Fused S1 (kNorm): bitmap, word offsets, error counts, tokens, staged
+    // block-table row, 16-byte aligned after `kind`.
+    uint32_t* n_bm = reinterpret_cast<uint32_t*>(
+        (reinterpret_cast<uintptr_t>(kind + cap) + 15) & ~uintptr_t(15));
+    int* n_wpos = reinterpret_cast<int*>(n_bm + hs_norm::kWindowWords);
+    int* n_err = n_wpos + hs_norm::kWindowWords;
+    int32_t* n_tok = n_err + 4;
+    int32_t* n_table = n_tok + cap;
 
     hs::pdl_trigger();
     const int row = blockIdx.x;
@@ -160,15 +173,57 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     int16_t* lru = a.lru + int64_t(row) * hot_size;
     const int64_t hot_base = int64_t(row) * a.region_stride;
 
-    // Every global read of the kernel is issued here, in one batch: the
-    // row's state, its pending ids and its count.
-    const int n = a.count ? min(max(a.count[row], 0), cap) : cap;
+    int n;
     const int32_t newest = a.newest_slot ? a.newest_slot[row] : -1;
-    for (int j = tid; j < hot_size; j += kThreads) {
-        s_dgi[j] = dgi[j];
-        s_lru[j] = lru[j];
+    if constexpr (kNorm) {
+        // The row's state lands in shared memory (16-byte cp.async) while the
+        // same CTA runs S1; S1's ascending slots go straight to `state`.
+        // 16-byte copies need 16-byte aligned rows on both sides (s_dgi sits
+        // at 8 * HS + 8 * cap bytes: cap even; the host checks the rest).
+        const bool async_ok = a.state_async &&
+                              ((hs::smem_u32(s_dgi) | hs::smem_u32(s_lru)) & 15u) == 0 &&
+                              ((reinterpret_cast<uintptr_t>(dgi) |
+                                reinterpret_cast<uintptr_t>(lru)) & 15u) == 0;
+        if (async_ok) {
+            for (int j = tid * 4; j < hot_size; j += kThreads * 4)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 hs::smem_u32(s_dgi + j)),
+                             "l"(dgi + j)
+                             : "memory");
+            for (int j = tid * 8; j < hot_size; j += kThreads * 8)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 hs::smem_u32(s_lru + j)),
+                             "l"(lru + j)
+                             : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        } else {
+            for (int j = tid; j < hot_size; j += kThreads) {
+                s_dgi[j] = dgi[j];
+                s_lru[j] = lru[j];
+            }
+        }
+        n = hs_norm::normalize_row<kThreads>(a.norm, row, a.norm.stage_table ? n_table : nullptr,
+                                             n_tok, state, n_bm, n_wpos, scan_scratch, n_err);
+        // S1's outputs, coalesced (the last emission is behind a barrier).
+        int32_t* g_tok = a.norm.out_tok + int64_t(row) * cap;
+        int32_t* g_slot = a.norm.out_slot + int64_t(row) * cap;
+        for (int j = tid; j < cap; j += kThreads) {
+            g_tok[j] = j < n ? n_tok[j] : -1;
+            g_slot[j] = j < n ? state[j] : -1;
+        }
+        if (tid == 0) a.norm.out_count[row] = n;
+        if (tid < 4) a.norm.err_counts[int64_t(row) * 4 + tid] = n_err[tid];
+        if (async_ok) asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        // Every global read of the kernel is issued here, in one batch: the
+        // row's state, its pending ids and its count.
+        n = a.count ? min(max(a.count[row], 0), cap) : cap;
+        for (int j = tid; j < hot_size; j += kThreads) {
+            s_dgi[j] = dgi[j];
+            s_lru[j] = lru[j];
+        }
+        for (int i = tid; i < cap; i += kThreads) state[i] = g_row[i];
     }
-    for (int i = tid; i < cap; i += kThreads) state[i] = g_row[i];
     if (tid == 0) s_dup = 0;
     __syncthreads();
 
@@ -193,8 +248,9 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     // Repeats of an earlier pending id resolve to -1.  This runs in the
     // same phase as the LRU walk below: the walk writes only first
     // occurrences (vals[h]) and this only later ones, and a first occurrence
-    // reads as pending or done here, never as a repeat.
-    {
+    // reads as pending or done here, never as a repeat.  S1's output (kNorm)
+    // is a set: no repeats to look for.
+    if constexpr (!kNorm) {
         int dups = 0;
         for (int i = tid; i < cap; i += kThreads) {
             const int32_t g = state[i];
@@ -390,11 +446,17 @@ extern "C" int hs_hot_state_reset(int32_t* dgi, int16_t* lru, int32_t rows, int3
 }
 
 namespace {
-template <bool kSwap>
+template <bool kSwap, bool kNorm = false>
 int lookup_launch(LookupArgs a, int32_t rows, int32_t cap, int32_t hot_size, hs_stream_t stream) {
     // Hash of load factor <= 1/4, or <= 1/2 when the larger table does not fit.
+    // Fused S1: bitmap, word offsets and tokens (+ the staged block-table row).
+    const size_t norm_bytes =
+        kNorm ? 16 + size_t(8) * hs_norm::kWindowWords + 16 + size_t(4) * cap +
+                    (a.norm.stage_table ? size_t(4) * a.norm.max_blocks : 0)
+              : 0;
     const auto smem_for = [&](int l2) {
-        return size_t(8) * (size_t(1) << l2) + size_t(9) * cap + size_t(10) * hot_size;
+        return size_t(8) * (size_t(1) << l2) + size_t(9) * cap + size_t(10) * hot_size +
+               norm_bytes;
     };
     int log2n = 6;
     while ((1 << log2n) < 4 * cap) ++log2n;
@@ -403,10 +465,11 @@ int lookup_launch(LookupArgs a, int32_t rows, int32_t cap, int32_t hot_size, hs_
     if (smem > size_t(kMaxSmem)) return HS_ERR_CAPACITY;
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(
-        reinterpret_cast<const void*>(lookup_kernel<kSwap>), smem, smem_set);
+        reinterpret_cast<const void*>(lookup_kernel<kSwap, kNorm>), smem, smem_set);
     if (rc != HS_OK) return rc;
     a.hash_log2 = log2n;
-    return hs_host::launch_pdl(lookup_kernel<kSwap>, dim3(rows), dim3(kThreads), smem, stream, a);
+    return hs_host::launch_pdl(lookup_kernel<kSwap, kNorm>, dim3(rows), dim3(kThreads), smem,
+                               stream, a);
 }
 }  // namespace
 
@@ -430,7 +493,7 @@ extern "C" int hs_hot_lookup_assign(const int32_t* slot, const int32_t* count, i
     LookupArgs a{slot,     count,    rows,     cap,        num_real_rows, newest_slot,
                  dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
                  miss_src, miss_dst, miss_count, stats,    err,           0,
-                 hit_idx,  miss_rows, nullptr, 0, nullptr, 0};
+                 hit_idx,  miss_rows, nullptr, 0, nullptr, 0, {}, 0};
     return lookup_launch<false>(a, rows, cap, hot_size, stream);
 }
 
@@ -463,6 +526,82 @@ extern "C" int hs_hot_lookup_swap_in(const int32_t* slot, const int32_t* count, 
                  dgi,      lru,      hot_size, region_stride, hot_idx,    miss_mask,
                  miss_src, miss_dst, miss_count, stats,    err,           0,
                  hit_idx,  miss_rows, static_cast<const uint8_t*>(host_pool), host_rows,
-                 static_cast<uint8_t*>(hot), row_bytes};
+                 static_cast<uint8_t*>(hot), row_bytes, {}, 0};
     return lookup_launch<true>(a, rows, cap, hot_size, stream);
+}
+
+extern "C" int hs_normalize_lookup_assign(
+    const int32_t* cand, int32_t rows, int32_t n_cand, int32_t window, int32_t num_sinks,
+    const int32_t* row_req, const int32_t* seq_lens, const int32_t* block_table,
+    int64_t bt_stride, int32_t max_blocks, const int32_t* page_owner, int32_t num_reqs,
+    int32_t num_pages, int32_t page_size, int32_t cap, int32_t* out_tok, int32_t* out_slot,
+    int32_t* out_count, int32_t* err_counts, const int32_t* newest_slot, int32_t* dgi,
+    int16_t* lru, int32_t hot_size, int64_t region_stride, int32_t* hot_idx, uint8_t* miss_mask,
+    int32_t* miss_src, int64_t* miss_dst, int32_t* miss_count, int64_t* stats, int32_t* err,
+    int32_t* hit_idx, int32_t* miss_rows, hs_stream_t stream) {
+    // S1's checks (as hs_normalize_indices) ...
+    if (rows < 0 || n_cand < 0 || window < 0 || num_sinks < 0 || max_blocks < 0 ||
+        num_reqs < 0 || num_pages < 0 || page_size <= 0 || cap < 0 || bt_stride < max_blocks)
+        return HS_ERR_INVALID_ARG;
+    if (int64_t(cap) < int64_t(n_cand) + window + num_sinks) return HS_ERR_CAPACITY;
+    if (int64_t(num_pages) * page_size > INT32_MAX) return HS_ERR_INVALID_ARG;
+    // ... and S2's (as hs_hot_lookup_assign).
+    if (hot_size <= 0 || hot_size > 32767) return HS_ERR_INVALID_ARG;
+    if (region_stride < int64_t(hot_size) + 1) return HS_ERR_INVALID_ARG;
+    if (int64_t(rows) * region_stride > INT32_MAX) return HS_ERR_INVALID_ARG;
+    if (cap > hot_size) return HS_ERR_CAPACITY;
+    if (rows == 0) return HS_OK;
+    if ((n_cand > 0 && cand == nullptr) || row_req == nullptr || out_tok == nullptr ||
+        out_slot == nullptr || out_count == nullptr || err_counts == nullptr)
+        return HS_ERR_INVALID_ARG;
+    if (num_reqs > 0 && (seq_lens == nullptr || (max_blocks > 0 && block_table == nullptr)))
+        return HS_ERR_INVALID_ARG;
+    if (dgi == nullptr || lru == nullptr ||
+        (cap > 0 && (hot_idx == nullptr || miss_src == nullptr || miss_dst == nullptr)) ||
+        miss_count == nullptr || stats == nullptr || err == nullptr)
+        return HS_ERR_INVALID_ARG;
+    hs_norm::NormArgs na{};
+    na.cand = cand;
+    na.rows = rows;
+    na.n_cand = n_cand;
+    na.window = window;
+    na.num_sinks = num_sinks;
+    na.row_req = row_req;
+    na.seq_lens = seq_lens;
+    na.block_table = block_table;
+    na.bt_stride = bt_stride;
+    na.max_blocks = max_blocks;
+    na.page_owner = page_owner;
+    na.num_reqs = num_reqs;
+    na.num_pages = num_pages;
+    na.page_size = page_size;
+    na.cap = cap;
+    na.out_tok = out_tok;
+    na.out_slot = out_slot;
+    na.out_count = out_count;
+    na.err_counts = err_counts;
+    na.stage_table = max_blocks <= hs_norm::kMaxStagedBlocks ? 1 : 0;
+    na.page_shift = -1;
+    na.stage_out = 1;
+    if ((page_size & (page_size - 1)) == 0) {
+        int sh = 0;
+        while ((1 << sh) < page_size) ++sh;
+        na.page_shift = sh;
+    }
+    // State rows copied with 16-byte cp.async: rows of a multiple of 8 slots,
+    // 16-byte aligned arrays, and an even cap (shared-memory offsets).
+    const bool aligned = hot_size % 8 == 0 && cap % 2 == 0 &&
+                         ((reinterpret_cast<uintptr_t>(dgi) | reinterpret_cast<uintptr_t>(lru)) &
+                          15u) == 0;
+    LookupArgs a{nullptr,  nullptr,  rows,     cap,        rows,       newest_slot,
+                 dgi,      lru,      hot_size, region_stride, hot_idx,  miss_mask,
+                 miss_src, miss_dst, miss_count, stats,    err,        0,
+                 hit_idx,  miss_rows, nullptr, 0, nullptr, 0, na, aligned ? 1 : 0};
+    int rc = lookup_launch<false, true>(a, rows, cap, hot_size, stream);
+    if (rc == HS_ERR_CAPACITY && na.stage_table) {
+        // Shared memory too small with the table staged: read it from global.
+        a.norm.stage_table = 0;
+        rc = lookup_launch<false, true>(a, rows, cap, hot_size, stream);
+    }
+    return rc;
 }

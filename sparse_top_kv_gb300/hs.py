@@ -37,6 +37,9 @@ _SIGS = {
     "hs_normalize_indices": ([_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _I32, _P, _I32, _I32,
                               _I32, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "hs_hot_state_reset": ([_P, _P, _I32, _I32, _P], ctypes.c_int),
+    "hs_normalize_lookup_assign": ([_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _I32, _P, _I32,
+                                    _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _I64,
+                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "hs_hot_lookup_assign": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I64, _P, _P, _P, _P,
                               _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "hs_layer_transfer": ([_P, _P, _I64, _I64, _I32, _I32, _I32, _I32, _I64, _I64, _P, _P, _I32,
@@ -174,6 +177,49 @@ def normalize_indices(cand, row_req, seq_lens, block_table, page_size, *, window
           num_pages, page_size, cap, _ptr(tok), _ptr(slot), _ptr(count), _ptr(err),
           _stream(stream))
     return tok, slot, count, err
+
+
+def normalize_lookup_assign(cand, row_req, seq_lens, block_table, page_size, newest_slot, dgi,
+                            lru, region_stride, stats, *, window=0, num_sinks=0, page_owner=None,
+                            num_pages, max_blocks=None, cap=None, s1_out=None, s2_out=None,
+                            stream=None):
+    """S1 and S2 in one kernel (hs_normalize_lookup_assign).  Returns
+    (s1_out, s2_out): (tok, slot, count, err) as normalize_indices and the
+    8-tuple (hot_idx, miss_mask, miss_src, miss_dst, miss_count, err,
+    hit_idx, miss_rows) as hot_lookup_assign with split lists."""
+    for t, n in ((cand, "cand"), (row_req, "row_req"), (seq_lens, "seq_lens"),
+                 (block_table, "block_table"), (page_owner, "page_owner"),
+                 (newest_slot, "newest_slot"), (dgi, "dgi")):
+        _check(t, torch.int32, n)
+    _check(lru, torch.int16, "lru")
+    _check(stats, torch.int64, "stats")
+    rows, n_cand = cand.shape
+    num_reqs, bt_stride = block_table.shape
+    max_blocks = bt_stride if max_blocks is None else max_blocks
+    cap = n_cand + window + num_sinks if cap is None else cap
+    hot_size = dgi.shape[1]
+    dev = cand.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    if s1_out is None:
+        s1_out = (torch.empty(rows, cap, **i32), torch.empty(rows, cap, **i32),
+                  torch.empty(rows, **i32), torch.empty(rows, 4, **i32))
+    if s2_out is None:
+        s2_out = (torch.empty(rows, cap, **i32),
+                  torch.empty(rows, cap, dtype=torch.uint8, device=dev),
+                  torch.empty(rows, cap, **i32),
+                  torch.empty(rows, cap, dtype=torch.int64, device=dev),
+                  torch.empty(rows, **i32), torch.empty(rows, **i32),
+                  torch.empty(rows, cap, **i32), torch.empty(rows, cap, **i32))
+    tok, slot, count, err = s1_out
+    hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr, hit_idx, miss_rows = s2_out
+    _call("hs_normalize_lookup_assign", _ptr(cand), rows, n_cand, window, num_sinks,
+          _ptr(row_req), _ptr(seq_lens), _ptr(block_table), bt_stride, max_blocks,
+          _ptr(page_owner), num_reqs, num_pages, page_size, cap, _ptr(tok), _ptr(slot),
+          _ptr(count), _ptr(err), _ptr(newest_slot), _ptr(dgi), _ptr(lru), hot_size,
+          region_stride, _ptr(hot_idx), _ptr(miss_mask), _ptr(miss_src), _ptr(miss_dst),
+          _ptr(miss_count), _ptr(stats), _ptr(lerr), _ptr(hit_idx), _ptr(miss_rows),
+          _stream(stream))
+    return s1_out, s2_out
 
 
 def hot_state_reset(dgi, lru, stream=None):

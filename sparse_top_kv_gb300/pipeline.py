@@ -3,8 +3,8 @@
 Stage order per step (vLLM HiSparse walkthrough, "swap_in 方法流程详解" and the
 BackUp interface of its overview):
   (model)  the new token's KV row lands in the request's reserved hot row
-  S1       hs_normalize_indices  candidates -> sorted unique slots
-  S2       hs_hot_lookup_assign  hot rows, misses, LRU update
+  S1 + S2  hs_normalize_lookup_assign  candidates -> sorted unique slots ->
+           hot rows, misses, LRU update (one kernel)
   S3       hs_swap_in            missed rows host -> hot;  hs_backup  reserved row -> host
   S4       hs_sparse_decode      attention over the hot rows
 Torch provides device memory, pinned host memory and the stream; every stage is
@@ -161,23 +161,23 @@ class HiSparseDecoder:
         swapped rows (miss_rows) follows the SwapIn, and the two sets of
         partial states are merged with eq. (7).  The new rows' write and
         their BackUp run on the side stream ahead of that attention.
-        `events`, if given, is a list of 7 CUDA events recorded before S1, after
-        S1, after S2, before and after SwapIn, after the resident-row attention
-        (side stream) and at the end of the step."""
+        `events`, if given, is a list of 7 CUDA events recorded before S1 + S2
+        (one kernel), after it (twice), before and after SwapIn, after the
+        resident-row attention (side stream) and at the end of the step."""
         R = self.num_reqs
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side
         rec = (lambda i, st: events[i].record(st)) if events is not None else (lambda i, st: None)
         rec(0, main)
-        tok, slot, count, err = hs.normalize_indices(
-            cand, self.row_req, seq_lens, self.block_table, self.page_size,
-            window=self.window, num_sinks=self.num_sinks, num_pages=self.num_pages,
-            out=self.s1_out, stream=main)
+        # S1 and S2 in one kernel (one CTA per request; S1's set stays in
+        # shared memory for the lookup).
+        (tok, slot, count, err), (hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr,
+                                  hit_idx, miss_rows) = hs.normalize_lookup_assign(
+            cand, self.row_req, seq_lens, self.block_table, self.page_size, newest_slot,
+            self.dgi, self.lru, self.region_stride, self.stats, window=self.window,
+            num_sinks=self.num_sinks, num_pages=self.num_pages, s1_out=self.s1_out,
+            s2_out=self.s2_out, stream=main)
         rec(1, main)
-        (hot_idx, miss_mask, miss_src, miss_dst, miss_count, lerr, hit_idx,
-         miss_rows) = hs.hot_lookup_assign(slot, count, newest_slot, self.dgi, self.lru,
-                                           self.region_stride, self.stats, out=self.s2_out,
-                                           stream=main)
         rec(2, main)
         self.ev_lists.record(main)
         # Main stream: the SwapIn of the misses right behind S2, then the
@@ -358,10 +358,10 @@ class HiSparseDecoder:
         return q if q.dtype == torch.bfloat16 else q.view(torch.bfloat16)
 
     # Kernels of libhs launched by one step (index_copy_ above is torch's):
-    # BackUp, S1, S2, SwapIn, resident-row attention, swapped-row attention
-    # with the merge in its epilogue.
+    # BackUp, S1 + S2 (one kernel), SwapIn, resident-row attention,
+    # swapped-row attention with the merge in its epilogue.
     def launches_per_step(self):
-        return 6
+        return 5
 
 
 class MultiLayerHiSparse:

@@ -106,3 +106,21 @@ def test_workspace_query_is_pure(rows, heads, cap):
     a = hs.sparse_decode_workspace_bytes(rows, heads, 1, cap, 576, 512)
     b = hs.sparse_decode_workspace_bytes(rows, heads, 1, cap, 576, 512)
     assert a == b and a >= 0
+
+
+def test_fused_normalize_lookup_argument_checks():
+    L = hs.lib()
+    P = None
+    # S1's checks: negative rows; cap below n_cand + window + sinks.
+    assert L.hs_normalize_lookup_assign(P, -1, 4, 0, 0, P, P, P, 4, 4, P, 1, 1, 64, 4, P, P, P, P,
+                                        P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P) == 1
+    assert L.hs_normalize_lookup_assign(P, 1, 4, 2, 1, P, P, P, 4, 4, P, 1, 1, 64, 6, P, P, P, P,
+                                        P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P) == 3
+    # S2's checks: cap > hot_size; region stride below hot_size + 1.
+    assert L.hs_normalize_lookup_assign(P, 1, 4, 0, 0, P, P, P, 4, 4, P, 1, 1, 64, 9, P, P, P, P,
+                                        P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P) == 3
+    assert L.hs_normalize_lookup_assign(P, 1, 4, 0, 0, P, P, P, 4, 4, P, 1, 1, 64, 4, P, P, P, P,
+                                        P, P, P, 8, 8, P, P, P, P, P, P, P, P, P, P) == 1
+    # Null outputs with rows > 0.
+    assert L.hs_normalize_lookup_assign(P, 1, 4, 0, 0, P, P, P, 4, 4, P, 1, 1, 64, 4, P, P, P, P,
+                                        P, P, P, 8, 9, P, P, P, P, P, P, P, P, P, P) == 1
