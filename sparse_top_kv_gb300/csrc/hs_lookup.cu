@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int32_t kEmpty = -1;
-constexpr int32_t kDone = INT32_MIN;
+constexpr int32_t kPend = -2;  // outv of an entry still looked for (hot rows are >= 0)
 constexpr uint8_t kNone = 0, kHit = 1, kMiss = 2;
 constexpr int kMaxSmem = 227 * 1024;
 
@@ -121,30 +121,38 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     const int hot_size = a.hot_size;
     int32_t* keys = reinterpret_cast<int32_t*>(smem);
     int32_t* vals = keys + HS;
-    int32_t* state = vals + HS;       // pending id, or kDone
-    int32_t* outv = state + cap;      // hot_idx value of each entry
+    int32_t* state = vals + HS;       // pending id of each entry whose outv is kPend
+    int32_t* outv = state + cap;      // hot_idx value of each entry, or kPend
     int32_t* s_dgi = outv + cap;
     int16_t* s_lru = reinterpret_cast<int16_t*>(s_dgi + hot_size);
     int16_t* E = s_lru + hot_size;
     int16_t* H = E + hot_size;
-    uint8_t* kind = reinterpret_cast<uint8_t*>(H + hot_size);  // kNone / kHit / kMiss
-    // Fused S1 (kNorm): bitmap, word offsets, error counts, tokens, staged
-    // block-table row, 16-byte aligned after `kind`.
+    // kMiss for misses and kHit for the newest row; other hits are told by
+    // outv >= 0 alone (one store per hit in the LRU walk).
+    uint8_t* kind = reinterpret_cast<uint8_t*>(H + hot_size);
+    // Fused S1 (kNorm): bitmap, word offsets, error counts, S1's tokens and
+    // slots (swizzled, cap rounded up to 32), staged block-table row; 16-byte
+    // aligned after `kind`.
+    const int cap32 = kNorm ? (cap + 31) & ~31 : 0;
     uint32_t* n_bm = reinterpret_cast<uint32_t*>(
         (reinterpret_cast<uintptr_t>(kind + cap) + 15) & ~uintptr_t(15));
     int* n_wpos = reinterpret_cast<int*>(n_bm + hs_norm::kWindowWords);
     int* n_err = n_wpos + hs_norm::kWindowWords;
     int32_t* n_tok = n_err + 4;
-    int32_t* n_table = n_tok + cap;
+    int32_t* n_slot = n_tok + cap32;
+    int32_t* n_table = n_slot + cap32;
 
     hs::pdl_trigger();
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
-    // Before the predecessor has completed: only the hash is cleared.
+    // Before the predecessor has completed: the hash (and S1's bitmap) are
+    // cleared.
     for (int h = tid * 4; h < HS; h += kThreads * 4) {
         *reinterpret_cast<int4*>(keys + h) = make_int4(kEmpty, kEmpty, kEmpty, kEmpty);
         *reinterpret_cast<int4*>(vals + h) = make_int4(INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX);
     }
+    if constexpr (kNorm)
+        for (int w = tid; w < hs_norm::kWindowWords; w += kThreads) n_bm[w] = 0u;
     hs::pdl_wait();
     const int32_t* g_row = a.slot + int64_t(row) * cap;
     int32_t* out = a.hot_idx + int64_t(row) * cap;
@@ -203,13 +211,15 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
             }
         }
         n = hs_norm::normalize_row<kThreads>(a.norm, row, a.norm.stage_table ? n_table : nullptr,
-                                             n_tok, state, n_bm, n_wpos, scan_scratch, n_err);
+                                             n_tok, n_slot, 31, n_bm, true, n_wpos, scan_scratch,
+                                             n_err);
         // S1's outputs, coalesced (the last emission is behind a barrier).
         int32_t* g_tok = a.norm.out_tok + int64_t(row) * cap;
         int32_t* g_slot = a.norm.out_slot + int64_t(row) * cap;
         for (int j = tid; j < cap; j += kThreads) {
-            g_tok[j] = j < n ? n_tok[j] : -1;
-            g_slot[j] = j < n ? state[j] : -1;
+            const int e = hs_norm::out_index(j, 31);
+            g_tok[j] = j < n ? n_tok[e] : -1;
+            g_slot[j] = j < n ? n_slot[e] : -1;
         }
         if (tid == 0) a.norm.out_count[row] = n;
         if (tid < 4) a.norm.err_counts[int64_t(row) * 4 + tid] = n_err[tid];
@@ -229,37 +239,36 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
 
     // Phase 1: classify entries, hash the pending ids (first occurrence wins).
     for (int i = tid; i < cap; i += kThreads) {
-        const int32_t g = i < n ? state[i] : -1;
-        if (g < 0) {
-            outv[i] = -1;
-            kind[i] = kNone;
-            state[i] = kDone;
-        } else if (newest >= 0 && g == newest) {
-            outv[i] = int32_t(hot_base + hot_size);
-            kind[i] = kHit;
-            state[i] = kDone;
-        } else {
+        int32_t g;
+        if constexpr (kNorm) g = i < n ? n_slot[hs_norm::out_index(i, 31)] : -1;
+        else g = i < n ? state[i] : -1;
+        int32_t v = -1;
+        uint8_t kd = kNone;
+        if (g >= 0 && newest >= 0 && g == newest) {
+            v = int32_t(hot_base + hot_size);
+            kd = kHit;
+        } else if (g >= 0) {
             const int h = insert_key(keys, g, a.hash_log2);
             if (h >= 0) atomicMin(&vals[h], i);
-            state[i] = g;
+            v = kPend;
+            if constexpr (kNorm) state[i] = g;
         }
+        outv[i] = v;
+        kind[i] = kd;
     }
     __syncthreads();
     // Repeats of an earlier pending id resolve to -1.  This runs in the
     // same phase as the LRU walk below: the walk writes only first
     // occurrences (vals[h]) and this only later ones, and a first occurrence
-    // reads as pending or done here, never as a repeat.  S1's output (kNorm)
+    // reads as pending or found here, never as a repeat.  S1's output (kNorm)
     // is a set: no repeats to look for.
     if constexpr (!kNorm) {
         int dups = 0;
         for (int i = tid; i < cap; i += kThreads) {
-            const int32_t g = state[i];
-            if (g == kDone) continue;
-            const int h = find_key(keys, g, a.hash_log2);
+            if (outv[i] != kPend) continue;
+            const int h = find_key(keys, state[i], a.hash_log2);
             if (h >= 0 && vals[h] != i) {
-                state[i] = kDone;
                 outv[i] = -1;
-                kind[i] = kNone;
                 ++dups;
             }
         }
@@ -285,8 +294,6 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
         if (h < 0) continue;
         const int i = vals[h];
         outv[i] = int32_t(hot_base + sl);
-        kind[i] = kHit;
-        state[i] = kDone;
         hitmask |= 1u << k;
         ++nh;
     }
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     for (int k = 0; k < K3; ++k) {
         const int i = i0 + k;
         if (i >= cap) break;
-        nm += state[i] != kDone;
+        nm += outv[i] == kPend;
     }
     int packed_total;
     const int packed = hs::block_excl_scan(nh | (nm << 16), scan_scratch, &packed_total);
@@ -326,8 +333,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     for (int k = 0; k < K3; ++k) {
         const int i = i0 + k;
         if (i >= cap) break;
+        if (outv[i] != kPend) continue;
         const int32_t g = state[i];
-        if (g == kDone) continue;
         const int16_t sl = m < nE ? E[m] : int16_t(-1);
         if (sl >= 0 && sl < hot_size) {
             outv[i] = int32_t(hot_base + sl);
@@ -354,7 +361,7 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const LookupArgs a) {
     // unused tails of the miss lists.
     for (int i = tid; i < cap; i += kThreads) {
         const int32_t v = outv[i];
-        const uint8_t kd = kind[i];
+        const uint8_t kd = v < 0 ? kNone : (kind[i] == kMiss ? kMiss : kHit);
         out[i] = v;
         if (hidx) hidx[i] = kd == kHit ? v : -1;
         if (mm) mm[i] = kd == kMiss ? 1 : 0;
@@ -451,7 +458,8 @@ int lookup_launch(LookupArgs a, int32_t rows, int32_t cap, int32_t hot_size, hs_
     // Hash of load factor <= 1/4, or <= 1/2 when the larger table does not fit.
     // Fused S1: bitmap, word offsets and tokens (+ the staged block-table row).
     const size_t norm_bytes =
-        kNorm ? 16 + size_t(8) * hs_norm::kWindowWords + 16 + size_t(4) * cap +
+        kNorm ? 16 + size_t(8) * hs_norm::kWindowWords + 16 +
+                    size_t(8) * ((size_t(cap) + 31) & ~size_t(31)) +
                     (a.norm.stage_table ? size_t(4) * a.norm.max_blocks : 0)
               : 0;
     const auto smem_for = [&](int l2) {

@@ -71,23 +71,35 @@ __device__ __forceinline__ int classify_in_range(int64_t t, const int32_t* table
     return -1;
 }
 
+// Index of output entry j in a shared-memory output array: with swz = 31
+// the low five bits are XORed with bits 5-9 (a permutation within every
+// aligned run of 1024 entries, so the array needs its length rounded up to
+// a multiple of 32).  A dense bitmap word puts 32 consecutive outputs on one
+// thread, so the threads of a warp write entries 32 apart: without the
+// swizzle those all fall on one bank.
+__device__ __forceinline__ int out_index(int j, int swz) { return j ^ ((j >> 5) & swz); }
+
 // Normalises index row `row` with the NT threads of the block (every thread
-// must call it): the ascending set of valid positions goes to otok[0 .. n)
-// and their slots to oslot[0 .. n) (shared or global memory), s_err[4]
-// receives the rejected-candidate counts; returns n.  s_table: [max_blocks]
-// shared ints when a.stage_table; bm / wpos: [kWindowWords] shared words;
-// scan_scratch: >= 33 shared ints.
+// must call it): the ascending set of valid positions goes to otok and their
+// slots to oslot, entry j at out_index(j, swz) (swz = 31 for shared-memory
+// targets, 0 for global ones), s_err[4] receives the rejected-candidate
+// counts; returns n.  s_table: [max_blocks] shared ints when a.stage_table;
+// bm / wpos: [kWindowWords] shared words, bm already zero when bm_zeroed
+// (the zeros written by the block before the call); scan_scratch: >= 33
+// shared ints.
 template <int NT>
 __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table, int32_t* otok,
-                             int32_t* oslot, uint32_t* bm, int* wpos, int* scan_scratch,
-                             int* s_err) {
+                             int32_t* oslot, int swz, uint32_t* bm, bool bm_zeroed, int* wpos,
+                             int* scan_scratch, int* s_err) {
     constexpr int kWpt = kWindowWords / NT;
     static_assert(kWpt * NT == kWindowWords, "bitmap words per thread");
     const int tid = threadIdx.x;
     const int32_t* cand = a.cand + int64_t(row) * a.n_cand;
-    // The first kUnroll candidates of this thread, loaded before anything
-    // else (their latency overlaps the request lookups below); later chunks,
-    // if any, are loaded where they are used.
+    // The request first (the table row and the length depend on it), then
+    // the first kUnroll candidates of this thread, whose latency overlaps
+    // the table's copy below; later chunks, if any, are loaded where they
+    // are used.
+    const int32_t req = a.row_req[row];
     int32_t tv0[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -95,24 +107,23 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
         tv0[u] = i < a.n_cand ? __ldg(cand + i) : -1;
     }
     if (tid < 4) s_err[tid] = 0;
-    __syncthreads();
+    const bool has_req = req >= 0 && req < a.num_reqs;
+    const int32_t* table = has_req ? a.block_table + int64_t(req) * a.bt_stride : nullptr;
+    if (has_req && a.stage_table) {
+        // One coalesced copy of the row; every later lookup hits shared memory.
+        for (int b = tid; b < a.max_blocks; b += NT) s_table[b] = __ldg(table + b);
+        table = s_table;
+    }
+    __syncthreads();  // s_err and the staged table
 
-    const int32_t req = a.row_req[row];
     int out_n = 0;
-    if (req < 0 || req >= a.num_reqs) {
+    if (!has_req) {
         // No request: each dynamic candidate is a range error.
         int bad = 0;
         for (int i = tid; i < a.n_cand; i += NT) bad += (cand[i] != -1);
         if (bad) atomicAdd(&s_err[0], bad);
     } else {
         const int64_t T = max(a.seq_lens[req], 0);
-        const int32_t* table = a.block_table + int64_t(req) * a.bt_stride;
-        if (a.stage_table) {
-            // One coalesced copy of the row; every later lookup hits shared memory.
-            for (int b = tid; b < a.max_blocks; b += NT) s_table[b] = __ldg(table + b);
-            __syncthreads();
-            table = s_table;
-        }
         const int64_t a_hi = hs::min64(a.num_sinks, T);        // sinks  [0, a_hi)
         const int64_t s2 = hs::max64(hs::max64(T - a.window, 0), a_hi);  // window [s2, T)
 
@@ -141,8 +152,10 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
         for (int64_t lo = 0; lo < T; lo += kWindowBits) {
             const int64_t hi = hs::min64(T, lo + kWindowBits);
             const int nw = int((hi - lo + 31) >> 5);
-            for (int w = tid; w < nw; w += NT) bm[w] = 0u;
-            __syncthreads();
+            if (lo > 0 || !bm_zeroed) {
+                for (int w = tid; w < nw; w += NT) bm[w] = 0u;
+                __syncthreads();
+            }
 
             int er = 0, eo = 0, ed = 0;
             // Structural candidates: sinks [0, a_hi) and window [s2, T) (disjoint).
@@ -220,8 +233,9 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
                     const int64_t t = base + b;
                     int32_t blk, off;
                     split_pos(t, a, &blk, &off);
-                    otok[pos] = int32_t(t);
-                    oslot[pos] = table[blk] * a.page_size + off;
+                    const int e = out_index(pos, swz);
+                    otok[e] = int32_t(t);
+                    oslot[e] = table[blk] * a.page_size + off;
                     ++pos;
                 }
             }

@@ -26,8 +26,8 @@ constexpr int kThreads = 512;
 constexpr int kMaxOutStageBytes = 160 * 1024;  // dynamic shared memory for table + outputs
 
 __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
-    // Dynamic: [max_blocks] table when a.stage_table, then [cap] tokens and
-    // [cap] slots when a.stage_out.
+    // Dynamic: [max_blocks] table when a.stage_table, then [cap32] tokens and
+    // [cap32] slots (cap rounded up to 32) when a.stage_out.
     extern __shared__ int32_t s_dyn[];
     __shared__ uint32_t bm[kWindowWords];
     __shared__ int wpos[kWindowWords];  // output offset of each bitmap word
@@ -35,25 +35,30 @@ __global__ void __launch_bounds__(kThreads) normalize_kernel(const NormArgs a) {
     __shared__ int s_err[4];
 
     hs::pdl_trigger();
+    const int tid = threadIdx.x;
+    // The first window's bitmap is cleared while the predecessor may still run.
+    for (int w = tid; w < kWindowWords; w += kThreads) bm[w] = 0u;
     hs::pdl_wait();
     const int row = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int64_t cap32 = (int64_t(a.cap) + 31) & ~int64_t(31);
     int32_t* const g_tok = a.out_tok + int64_t(row) * a.cap;
     int32_t* const g_slot = a.out_slot + int64_t(row) * a.cap;
     int32_t* const s_table = s_dyn;
     int32_t* const s_tok = s_dyn + (a.stage_table ? a.max_blocks : 0);
-    int32_t* const s_slot = s_tok + a.cap;
-    // Emission targets: shared memory (written out coalesced at the end) or
-    // the global rows directly.
+    int32_t* const s_slot = s_tok + cap32;
+    // Emission targets: shared memory (swizzled, written out coalesced at the
+    // end) or the global rows directly.
     int32_t* const otok = a.stage_out ? s_tok : g_tok;
     int32_t* const oslot = a.stage_out ? s_slot : g_slot;
-    const int out_n = normalize_row<kThreads>(a, row, s_table, otok, oslot, bm, wpos,
+    const int out_n = normalize_row<kThreads>(a, row, s_table, otok, oslot,
+                                              a.stage_out ? 31 : 0, bm, true, wpos,
                                               scan_scratch, s_err);
     if (a.stage_out) {
         __syncthreads();
         for (int j = tid; j < a.cap; j += kThreads) {
-            g_tok[j] = j < out_n ? s_tok[j] : -1;
-            g_slot[j] = j < out_n ? s_slot[j] : -1;
+            const int e = out_index(j, 31);
+            g_tok[j] = j < out_n ? s_tok[e] : -1;
+            g_slot[j] = j < out_n ? s_slot[e] : -1;
         }
     } else {
         for (int j = out_n + tid; j < a.cap; j += kThreads) {
@@ -98,9 +103,10 @@ extern "C" int hs_normalize_indices(const int32_t* cand, int32_t rows, int32_t n
     }
     size_t smem = a.stage_table ? size_t(max_blocks) * sizeof(int32_t) : 0;
     // Outputs assembled in shared memory when they fit beside the table.
-    if (smem + size_t(cap) * 2 * sizeof(int32_t) <= size_t(kMaxOutStageBytes)) {
+    const size_t out_bytes = size_t((int64_t(cap) + 31) & ~int64_t(31)) * 2 * sizeof(int32_t);
+    if (smem + out_bytes <= size_t(kMaxOutStageBytes)) {
         a.stage_out = 1;
-        smem += size_t(cap) * 2 * sizeof(int32_t);
+        smem += out_bytes;
     }
     static int smem_set[64] = {};
     const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(normalize_kernel),
