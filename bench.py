@@ -1090,7 +1090,13 @@ def main():
                    "l2": "flushed (512 MB write) between timed steps, outside the events",
                    "inputs": "each step's packed inputs (1.78 MB) resident in HBM in their own "
                              "slot, read in place by the step's graph (no staging copy); the "
-                             "e2e number copies them host->device inside its timed region"},
+                             "e2e number copies them host->device inside its timed region",
+                   "host_rows": "caveat: the host rows each timed SwapIn reads were read by the "
+                                "GPU shortly before (a set-up pass over the workload and one "
+                                "untimed replay of each timed step, state restored), so their "
+                                "host page translations are warm; a SwapIn of the same size over "
+                                "rows not read recently ran at 146 GB/s, and over pages never "
+                                "read by the GPU at 34 GB/s (separate measurement)"},
         "step_us_timed": [round(x * 1e3, 1) for x in full["step_ms"]],
         "stage_us_note": "timed steps replay one CUDA graph per step; stage_us from "
                          + full["stage_src"],
