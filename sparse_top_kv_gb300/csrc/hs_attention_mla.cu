@@ -51,6 +51,12 @@ constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;  // 352 (168 registers per thread)
 constexpr int kLoadRows = kTok * 8 / (kLoadWarps * 32);  // rows per loader thread and block
 constexpr int kLoaderThreads = kLoadWarps * 32;
+constexpr int kSoftThreads = kSoftWarps * 32;
+// Threads that fill the first tile's QK units: the loaders and the softmax
+// warps (which have nothing to do before the first logits).  Every ring
+// barrier counts this many arrivals; a unit the loaders fill alone gets the
+// softmax threads' share from one loader thread.
+constexpr int kFillThreads = kLoaderThreads + kSoftThreads;
 constexpr int kHalfThreads = kSoftWarps * 16;  // softmax threads of one head half
 constexpr float kThresh = 8.0f;     // log2 headroom before O is rescaled
 constexpr int kMaxCombine = 4;      // partial columns a finishing pass can merge
@@ -165,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
     hs::pdl_trigger();
     if (tid == 0) {
         for (int i = 0; i < NU; ++i) {
-            hs::mbar_init(&B.full[i][0], kLoaderThreads);
-            hs::mbar_init(&B.full[i][1], kLoaderThreads);
+            hs::mbar_init(&B.full[i][0], kFillThreads);
+            hs::mbar_init(&B.full[i][1], kFillThreads);
             hs::mbar_init(&B.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -198,6 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
         hs::tc::cp_async_wait_all();
         hs::fence_proxy_async_shared();
     }
+    // The count and this row's candidate ids may still be written by a stream
+    // predecessor: an L2 prefetch (it returns no data) of their lines lets the
+    // loads after the wait hit L2.
+    {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(kv_rows) & ~uintptr_t(127);
+        const uintptr_t hi = reinterpret_cast<uintptr_t>(kv_rows + a.cap);
+        for (uintptr_t p = lo + uintptr_t(tid) * 128; p < hi; p += uintptr_t(kThreads) * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        if (tid == 0 && a.count != nullptr)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.count + row));
+    }
     hs::pdl_wait();
     const int n = a.count ? min(max(a.count[row], 0), a.cap) : a.cap;
     const int ntiles = (n + kTok - 1) / kTok;
@@ -213,6 +230,48 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
     __syncthreads();
     hs::tc::fence_after_sync();
     const uint32_t tmem = B.tmem_base;
+    // The first tile's QK units that own their ring slot (units k < NU, phase
+    // 0: no wait for a release), filled by the loader and softmax threads
+    // together; `gt` in [0, kFillThreads) takes the 16-byte chunks e = gt +
+    // kFillThreads i of every block (row e / 8, chunk e % 8).
+    constexpr int kFirstUnits = NU < kQkUnits ? NU : kQkUnits;
+    auto fill_first = [&](int gt) {
+        constexpr int kPer = (kTok * 8 + kFillThreads - 1) / kFillThreads;
+        const int jt = t_begin * kTok;
+        int32_t id[kPer];
+        bool bad0 = false;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = gt + kFillThreads * i;
+            const int j = jt + (e >> 3);
+            id[i] = (e < kTok * 8 && j < n) ? __ldg(kv_rows + j) : -1;
+            if (int64_t(id[i]) >= a.num_kv_rows) bad0 = true;
+        }
+#pragma unroll 1
+        for (int u = 0; u < kFirstUnits; ++u) {
+            const uint32_t ub = ring_base + u * kUnit;
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+                const int blk = 2 * u + bb;
+                if (blk >= kNB) break;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int e = gt + kFillThreads * i;
+                    if (e >= kTok * 8) continue;
+                    const int r = e >> 3, c = e & 7;
+                    const bool v = id[i] >= 0 && int64_t(id[i]) < a.num_kv_rows;
+                    const char* src = reinterpret_cast<const char*>(a.kv) +
+                                      (v ? int64_t(id[i]) : 0) * a.row_stride * 2 + blk * 128 +
+                                      c * 16;
+                    hs::tc::cp_async16(ub + bb * kBlk + r * 128 + ((c ^ (r & 7)) << 4), src,
+                                       v ? 16u : 0u);
+                }
+            }
+            hs::tc::cp_async_arrive_noinc(&B.full[u][0]);
+            hs::tc::cp_async_arrive_noinc(&B.full[u][1]);
+        }
+        if (bad0) hs::set_status(a.status, HS_ERR_BAD_INDEX);
+    };
 
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ------------------------------ loaders ------------------------------
@@ -253,14 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             hs::tc::cp_async_arrive_noinc(&B.full[slot][0]);
             // The second block's barrier completes its phase in every unit.
             hs::tc::cp_async_arrive_noinc(&B.full[slot][1]);
+            if (lt == 0) {
+                // The softmax threads' share of the arrivals (they fill only
+                // the first tile's units).
+                hs::mbar_arrive_count(&B.full[slot][0], kSoftThreads);
+                hs::mbar_arrive_count(&B.full[slot][1], kSoftThreads);
+            }
             return true;
         };
-        auto load_qk = [&](int t, const int32_t (&id)[kLoadRows]) -> bool {
+        auto load_qk = [&](int t, const int32_t (&id)[kLoadRows], int u0) -> bool {
 #pragma unroll
             for (int i = 0; i < kLoadRows; ++i)
                 if (int64_t(id[i]) >= a.num_kv_rows) bad = true;
             const int k0 = unit_seq(t, 0, 0, T);
-            for (int u = 0; u < kQkUnits; ++u)
+            for (int u = u0; u < kQkUnits; ++u)
                 if (!fill(k0 + u, id, u < 4 ? 2 * u : 8, u < 4 ? 2 * u + 1 : -1)) return false;
             return true;
         };
@@ -273,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
         fetch(0, id_cur);
         fetch(1, id_next);
         fetch(2, id_far);
-        bool ok = T == 0 || load_qk(0, id_cur);
+        if (T > 0) fill_first(kSoftThreads + lt);
+        bool ok = T == 0 || load_qk(0, id_cur, kFirstUnits);
         for (int t = 0; t < T && ok; ++t) {
             // id_prev = tile t, id_cur = t + 1, id_next = t + 2, id_far = t + 3.
 #pragma unroll
@@ -283,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                 id_next[i] = id_far[i];
             }
             fetch(t + 3, id_far);
-            if (t + 1 < T) ok = load_qk(t + 1, id_cur);
+            if (t + 1 < T) ok = load_qk(t + 1, id_cur, 0);
             if (ok && !reuse_v) ok = load_pv(t, id_prev);
         }
         if (!ok) {
@@ -372,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
         const int ht = qd * 32 + lane;      // thread index within the half
         const int hoff = hf * HH;           // first head (within the group) of the half
         const uint32_t lane_base = uint32_t(qd * 32) << 16;
+        if (T > 0) fill_first(tid);
         // The reference maxima are the same for every thread of the half:
         // they live in shared memory (buffer msel), written by thread 0 of
         // the half into the other buffer when a tile rescales.
@@ -517,7 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
             hs::tc::fence_before_sync();
             hs::mbar_arrive(&B.p_full);
         }
-        // Epilogue.
+        // Epilogue.  (This thread's copies of the first tile are complete
+        // before the CTA can exit.)
+        hs::tc::cp_async_wait_all();
         if (ok && T > 0) {
             ok = hs::mbar_wait_bounded(&B.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, tmo,
                                        abort_flag);
@@ -668,22 +737,27 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                         __threadfence();
                         const int nc = min(a.merge_total, kMlaMaxMerge);
                         if (ht < HH) {
+                            // Every column's (m, l) in one round of loads.
                             const int64_t qh = qh0 + hoff + ht;
                             const int64_t base = qh * a.part_stride;
                             float* w = B.cw[hoff + ht];
+                            float mc[kMlaMaxMerge], lc[kMlaMaxMerge];
+#pragma unroll
+                            for (int c = 0; c < kMlaMaxMerge; ++c) {
+                                lc[c] = c < nc ? __ldcg(a.part_l + base + c) : 0.f;
+                                mc[c] = c < nc ? __ldcg(a.part_m + base + c) : -CUDART_INF_F;
+                            }
                             float M = -CUDART_INF_F;
-                            for (int c = 0; c < nc; ++c)
-                                if (__ldcg(a.part_l + base + c) > 0.f)
-                                    M = fmaxf(M, __ldcg(a.part_m + base + c));
+#pragma unroll
+                            for (int c = 0; c < kMlaMaxMerge; ++c)
+                                if (lc[c] > 0.f) M = fmaxf(M, mc[c]);
                             float Lt = 0.f;
+#pragma unroll
                             for (int c = 0; c < kMlaMaxMerge; ++c) {
                                 float wc = 0.f;
-                                if (c < nc && M != -CUDART_INF_F) {
-                                    const float lc = __ldcg(a.part_l + base + c);
-                                    if (lc > 0.f) {
-                                        wc = exp2f(__ldcg(a.part_m + base + c) - M);
-                                        Lt = fmaf(wc, lc, Lt);
-                                    }
+                                if (lc[c] > 0.f && M != -CUDART_INF_F) {
+                                    wc = exp2f(mc[c] - M);
+                                    Lt = fmaf(wc, lc[c], Lt);
                                 }
                                 w[c] = wc;
                             }
@@ -697,37 +771,48 @@ __global__ void __launch_bounds__(kThreads, 1) mla_tc_kernel(const MlaArgs a) {
                             B.abort = 1;
                         } else {
                             // 16-byte chunks of d (128 per head), distributed over the
-                            // half's 128 threads; eight chunks in flight per thread.
+                            // half's 128 threads, kPer chunks per thread and pass; the
+                            // loads of up to four columns are in flight at once, and
+                            // each chunk accumulates the columns in order.
                             constexpr int kChunks = HH * 128;
+                            constexpr int kPer = 4;
 #pragma unroll 1
-                            for (int e0 = ht; e0 < kChunks; e0 += 8 * kHalfThreads) {
-                                float4 acc[8];
+                            for (int e0 = ht; e0 < kChunks; e0 += kPer * kHalfThreads) {
+                                float4 acc[kPer];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                for (int c = 0; c < nc; ++c) {
-                                    float4 v[8];
+                                for (int i = 0; i < kPer; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                                for (int c0 = 0; c0 < nc; c0 += 4) {
+                                    float4 v[4][kPer];
 #pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        const int e = e0 + i * kHalfThreads;
-                                        const int64_t qh = qh0 + hoff + e / 128;
-                                        v[i] = e < kChunks
-                                                   ? __ldcg(reinterpret_cast<const float4*>(
-                                                                a.part_o + (qh * a.part_stride + c) * 512) +
-                                                            (e & 127))
-                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+                                        for (int i = 0; i < kPer; ++i) {
+                                            const int e = e0 + i * kHalfThreads;
+                                            const int64_t qh = qh0 + hoff + e / 128;
+                                            v[cc][i] = c0 + cc < nc && e < kChunks
+                                                           ? __ldcg(reinterpret_cast<const float4*>(
+                                                                        a.part_o + (qh * a.part_stride + c0 + cc) * 512) +
+                                                                    (e & 127))
+                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                                        }
                                     }
 #pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        const int e = e0 + i * kHalfThreads;
-                                        const float wc = e < kChunks ? B.cw[hoff + e / 128][c] : 0.f;
-                                        acc[i].x = fmaf(wc, v[i].x, acc[i].x);
-                                        acc[i].y = fmaf(wc, v[i].y, acc[i].y);
-                                        acc[i].z = fmaf(wc, v[i].z, acc[i].z);
-                                        acc[i].w = fmaf(wc, v[i].w, acc[i].w);
+                                    for (int cc = 0; cc < 4; ++cc) {
+                                        if (c0 + cc >= nc) break;
+#pragma unroll
+                                        for (int i = 0; i < kPer; ++i) {
+                                            const int e = e0 + i * kHalfThreads;
+                                            const float wc = e < kChunks ? B.cw[hoff + e / 128][c0 + cc] : 0.f;
+                                            acc[i].x = fmaf(wc, v[cc][i].x, acc[i].x);
+                                            acc[i].y = fmaf(wc, v[cc][i].y, acc[i].y);
+                                            acc[i].z = fmaf(wc, v[cc][i].z, acc[i].z);
+                                            acc[i].w = fmaf(wc, v[cc][i].w, acc[i].w);
+                                        }
                                     }
                                 }
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) {
+                                for (int i = 0; i < kPer; ++i) {
                                     const int e = e0 + i * kHalfThreads;
                                     if (e >= kChunks) continue;
                                     const int hl = hoff + e / 128;

@@ -727,21 +727,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const float Lown = B.l_out[st] + B.l_in[st];
                         const float Mown = B.mref[msel][st];
                         const float* ml = a.part_m + (int64_t(rank) * a.rows * kHeads + qh) * a.splits * 2;
-                        float M = Lown > 0.f ? Mown : -CUDART_INF_F;
-                        for (int sp = 0; sp < a.splits; ++sp) {
-                            if (sp == split) continue;
-                            if (__ldcg(ml + sp * 2 + 1) > 0.f) M = fmaxf(M, __ldcg(ml + sp * 2));
+                        // Every split's (m, l) in one round of loads.
+                        float msp[kMlaPairMaxSplits], lsp[kMlaPairMaxSplits];
+#pragma unroll
+                        for (int sp = 0; sp < kMlaPairMaxSplits; ++sp) {
+                            const bool other = sp < a.splits && sp != split;
+                            const float2 v = other ? __ldcg(reinterpret_cast<const float2*>(ml + sp * 2))
+                                                   : make_float2(Mown, Lown);
+                            msp[sp] = v.x;
+                            lsp[sp] = sp < a.splits ? v.y : 0.f;
                         }
+                        float M = Lown > 0.f ? Mown : -CUDART_INF_F;
+#pragma unroll
+                        for (int sp = 0; sp < kMlaPairMaxSplits; ++sp)
+                            if (sp < a.splits && sp != split && lsp[sp] > 0.f) M = fmaxf(M, msp[sp]);
                         float Lt = 0.f;
-                        for (int sp = 0; sp < a.splits; ++sp) {
+#pragma unroll
+                        for (int sp = 0; sp < kMlaPairMaxSplits; ++sp) {
+                            if (sp >= a.splits) break;
                             float wsp = 0.f;
-                            if (M != -CUDART_INF_F) {
-                                const float lsp = sp == split ? Lown : __ldcg(ml + sp * 2 + 1);
-                                const float msp = sp == split ? Mown : __ldcg(ml + sp * 2);
-                                if (lsp > 0.f) {
-                                    wsp = exp2f(msp - M);
-                                    Lt = fmaf(wsp, lsp, Lt);
-                                }
+                            if (M != -CUDART_INF_F && lsp[sp] > 0.f) {
+                                wsp = exp2f(msp[sp] - M);
+                                Lt = fmaf(wsp, lsp[sp], Lt);
                             }
                             cw[st * kMlaPairMaxSplits + sp] = wsp;
                         }
@@ -754,33 +761,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 2; ++j) {
                         const int d = 256 * j + 128 * int(rank) + tl;
 #pragma unroll 1
-                        for (int c = 0; c < kHalfHeads; c += 16) {
-                            float o[16];
+                        for (int c = 0; c < kHalfHeads; c += 32) {
+                            float o[32];
                             if (T > 0) {
-                                hs::tc::tmem_ld16(tmem + lane_base + kO + j * kHeads + hf * kHalfHeads + c, o);
+                                hs::tc::tmem_ld16(tmem + lane_base + kO + j * kHeads + hf * kHalfHeads + c,
+                                                  *reinterpret_cast<float(*)[16]>(o));
+                                hs::tc::tmem_ld16(tmem + lane_base + kO + j * kHeads + hf * kHalfHeads + c + 16,
+                                                  *reinterpret_cast<float(*)[16]>(o + 16));
                                 hs::tc::tmem_wait_ld();
                             } else {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) o[i] = 0.f;
+                                for (int i = 0; i < 32; ++i) o[i] = 0.f;
                             }
-                            float acc[16];
+                            float acc[32];
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
+                            for (int i = 0; i < 32; ++i)
                                 acc[i] = cw[(hf * kHalfHeads + c + i) * kMlaPairMaxSplits + split] * o[i];
-                            // The other splits' partial outputs: 16 independent
+                            // The other splits' partial outputs: 32 independent
                             // loads per split in flight.
                             for (int sp = 0; sp < a.splits; ++sp) {
                                 if (sp == split) continue;
-                                float po[16];
+                                float po[32];
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
+                                for (int i = 0; i < 32; ++i)
                                     po[i] = __ldcg(a.part_o + ((qh0 + hf * kHalfHeads + c + i) * a.splits + sp) * 512 + d);
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
+                                for (int i = 0; i < 32; ++i)
                                     acc[i] = fmaf(cw[(hf * kHalfHeads + c + i) * kMlaPairMaxSplits + sp], po[i], acc[i]);
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
+                            for (int i = 0; i < 32; ++i) {
                                 const int g = hf * kHalfHeads + c + i;
                                 a.out[(qh0 + g) * 512 + d] = __float2bfloat16_rn(acc[i] * cinv[g]);
                             }

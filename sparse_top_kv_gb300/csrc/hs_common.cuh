@@ -53,6 +53,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
         : "memory");
 }
 
+// `count` arrivals at once (a thread standing in for others).
+__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(count)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile(
         "{\n\t.reg .b64 st;\n\t"
