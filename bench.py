@@ -34,7 +34,7 @@ ROW_BYTES = 1152
 FP8DS_ROW_BYTES = 656
 # DRAM bytes (read + write) per launch from an ncu capture of the same
 # launches (set to None when a kernel changes after the capture).
-NCU_TRAFFIC = {"attention": None, "swap_in": 385536 + 9796864}
+NCU_TRAFFIC = {"attention": 131877376 + 20214784, "swap_in": 283904 + 10095616}
 
 
 def load_peaks():
