@@ -304,7 +304,10 @@ int hs_layer_transfer(void* const* dev_layers, void* host_pool, int64_t host_tok
  *            bytes (split-KV partial states, and one arrival counter per
  *            (row, kv head, head group), zeroed by the call, so that the
  *            split that finishes last merges the others in its epilogue
- *            instead of a second launch); may be NULL when that is 0.
+ *            instead of a second launch); may be NULL when that is 0.  With
+ *            128 MLA heads and two splits per row, when every row's cluster
+ *            of four CTAs fits on the GPU at once, the two splits merge
+ *            through distributed shared memory and the size is 0.
  * status     int32 device word or NULL (HS_ERR_TIMEOUT from bounded waits,
  *            HS_ERR_BAD_INDEX from skipped rows).
  * Supported shapes: (d_qk, d_v) = (576, 512) with kv_heads == 1 and k_base

@@ -398,9 +398,12 @@ int64_t pair_part_ml_bytes(const Plan& p, int rows) {
 
 int64_t workspace_bytes(const Plan& p, int rows, int heads, int d_v) {
     if (p.kind == 0 || p.splits <= 1) return 0;
-    if (p.kind == 4)
+    if (p.kind == 4) {
+        // A row's two splits merged inside one cluster need no scratch.
+        if (mla_pair_cluster_merge(rows, p.splits)) return 0;
         return pair_part_o_bytes(p, rows) + pair_part_ml_bytes(p, rows) +
                (int64_t(rows) * 4 * 4 + 15) / 16 * 16;
+    }
     int64_t b = partial_bytes(p, rows, heads, d_v);
     if (p.kind == 3 || p.kind == 2) b += (sync_words(p, rows) * 4 + 15) / 16 * 16;
     return b;
@@ -868,7 +871,7 @@ int decode_impl(const void* q, const void* k_base, const void* v_base, int64_t r
             m.splits = p.splits;
             m.status = status;
             m.timeout_ns = hs::kWaitTimeoutNs;
-            if (p.splits > 1) {
+            if (p.splits > 1 && !mla_pair_cluster_merge(rows, p.splits)) {
                 unsigned char* w = static_cast<unsigned char*>(workspace);
                 m.part_o = reinterpret_cast<float*>(w);
                 m.part_m = reinterpret_cast<float*>(w + pair_part_o_bytes(p, rows));

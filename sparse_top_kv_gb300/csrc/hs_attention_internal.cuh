@@ -47,6 +47,9 @@ constexpr int kMlaPairMaxSplits = 8;
 // part_m = [2, rows * 128, splits, 2] fp32 (m, l per CTA rank), sync =
 // [rows, 2, 2] int32 counters, zero on entry and left zero.
 int launch_mla_pair(const MlaArgs& a, int pairs, hs_stream_t stream);
+// True when launch_mla_pair merges a row's two splits inside a cluster of
+// four CTAs (no partial states or counters in global memory).
+bool mla_pair_cluster_merge(int rows, int splits);
 
 // Query heads handled by one CTA (64, 32 or 16), or 0 when heads % 16 != 0.
 int mla_tc_head_group(int heads);

@@ -110,6 +110,8 @@ struct Bars {
     alignas(16) float l_in[kHeads];
     alignas(16) float mref[2][kHeads];   // reference maxima (log2 units), double buffered
     alignas(16) float alpha[kHeads];
+    alignas(16) float mlc[2][kHeads];    // cluster merge: this pair's (m, l) per head
+    float cwc[kHalfHeads][3];            // cluster merge: w(split 0), w(split 1), 1 / L
     float red[4][kHeads];    // per TMEM lane quarter: warp maxima or sums
 };
 constexpr int kSmemBytes = kBarOff + int(sizeof(Bars)) + 1024;
@@ -178,8 +180,14 @@ __device__ __forceinline__ int unit_seq(int t, int is_pv, int u, int T) {
     return kQkUnits + t * (kQkUnits + kPvUnits) + (t + 1 < T ? kQkSplit : 0) + u;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// CL = 2: one pair per cluster.  CL = 4 (a row split in two): the row's two
+// pairs form one cluster (ranks 2 s + r for split s) and merge through
+// distributed shared memory; the pair forms of tcgen05 pair the CTAs whose
+// cluster ranks differ in bit 0.
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     mla_pair_kernel(const MlaArgs a) {
+    constexpr bool kClusterMerge = CL == 4;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -190,8 +198,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t p_base = s_base + kPOff;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = pr::cta_rank();
-    const uint32_t peer = rank ^ 1u;
+    const uint32_t crank = pr::cta_rank();        // rank in the cluster
+    const uint32_t rank = crank & 1u;             // rank in the pair
+    const uint32_t peer = crank ^ 1u;             // the other CTA of the pair
+    const uint32_t pair_base = crank & ~1u;       // the pair's even CTA
+    const uint16_t pmask = uint16_t(3u << pair_base);
     const int pair_id = blockIdx.x >> 1;
     const int row = pair_id / a.splits;
     const int split = pair_id % a.splits;
@@ -366,9 +377,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint64_t bd = hs::tc::sdesc_sw128(q_base + b * kQBlk + kk * 32, 16, 1024);
                         pr::mma2_bf16(tmem + kS + sb * kHeads, ad, bd, idesc_qk, (b | kk) ? 1u : 0u);
                     }
-                    if ((b & 1) || b == kNB - 1) pr::commit2_both(&B.empty[k % kNU]);
+                    if ((b & 1) || b == kNB - 1) pr::commit2_both(&B.empty[k % kNU], pmask);
                 }
-                if (u1 == kQkUnits && u0 < u1) pr::commit2_both(&B.s_full[sb]);
+                if (u1 == kQkUnits && u0 < u1) pr::commit2_both(&B.s_full[sb], pmask);
                 return true;
             };
             auto issue_pv = [&](int t) -> bool {
@@ -391,9 +402,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         pr::mma2_bf16(tmem + kO + j * kHeads, ad, bd, idesc_pv,
                                       (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
                     }
-                    pr::commit2_both(&B.empty[k % kNU]);
+                    pr::commit2_both(&B.empty[k % kNU], pmask);
                 }
-                pr::commit2_both(&B.pv_done[t & 1]);
+                pr::commit2_both(&B.pv_done[t & 1], pmask);
                 return true;
             };
             bool ok = T == 0 || issue_qk(0, 0, kQkUnits);
@@ -404,12 +415,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (!ok) fail();
             // Drain: every pair MMA has completed before tensor memory is freed.
-            pr::commit2_both(&B.drain);
+            pr::commit2_both(&B.drain, pmask);
             pr::mbar_wait(&B.drain, 0, tmo, nullptr);
         } else if (lane == 0) {
             // ---------- relay (odd CTA): this CTA's units and P^T ready -------
-            const uint32_t r_pfull = pr::mapa(hs::smem_u32(&B.pfull[0]), 0);
-            const uint32_t r_ppeer = pr::mapa(hs::smem_u32(&B.p_peer), 0);
+            const uint32_t r_pfull = pr::mapa(hs::smem_u32(&B.pfull[0]), pair_base);
+            const uint32_t r_ppeer = pr::mapa(hs::smem_u32(&B.p_peer), pair_base);
             auto relay = [&](int k) -> bool {
                 const int slot = k % kNU;
                 if (!pr::mbar_wait(&B.full[slot][0], (k / kNU) & 1, tmo, abort_flag)) return false;
@@ -650,7 +661,114 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             ok = pr::mbar_wait(&B.l_full, 0, tmo, abort_flag);
         }
-        if (!ok) {
+        if constexpr (kClusterMerge) {
+            // The row's two splits are the two pairs of this cluster: every CTA
+            // parks its unnormalised O (its 256 d rows, all heads, [head][d
+            // row] in the idle ring and query space) and its pair's (m, l);
+            // after a cluster barrier that every thread of the cluster passes
+            // once here (the other warps at their end), CTA (s, r) merges
+            // heads [64 s, 64 s + 64) of its d rows from both splits with
+            // eq. (7), split 0's part first.
+            float* os = reinterpret_cast<float*>(smem + kRingOff);
+            const int64_t qh0 = int64_t(row) * kHeads;
+            if (!ok) {
+                fail();
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll 1
+                    for (int c = 0; c < kHalfHeads; c += 16) {
+                        float o[16];
+                        if (T > 0) {
+                            hs::tc::tmem_ld16(tmem + lane_base + kO + j * kHeads + hf * kHalfHeads + c, o);
+                            hs::tc::tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) o[i] = 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            os[(hf * kHalfHeads + c + i) * 256 + j * 128 + tl] = o[i];
+                    }
+                }
+                if (st < kHeads) {
+                    const float L = B.l_out[st] + B.l_in[st];
+                    B.mlc[0][st] = L > 0.f ? B.mref[msel][st] : -CUDART_INF_F;
+                    B.mlc[1][st] = L;
+                }
+            }
+            pr::cluster_sync();
+            const uint32_t other = crank ^ 2u;  // the other split's CTA of this rank
+            const bool merge_ok =
+                *abort_flag == 0 && pr::ld_remote_s32(pr::mapa(hs::smem_u32(&B.abort), other)) == 0;
+            if (merge_ok) {
+                const int sp = split;  // 0 or 1
+                if (st < kHalfHeads) {
+                    const int h = kHalfHeads * sp + st;
+                    const float mo = B.mlc[0][h], lo = B.mlc[1][h];
+                    const float mr = pr::ld_remote_f32(pr::mapa(hs::smem_u32(&B.mlc[0][h]), other));
+                    const float lr = pr::ld_remote_f32(pr::mapa(hs::smem_u32(&B.mlc[1][h]), other));
+                    const float m0 = sp == 0 ? mo : mr, l0 = sp == 0 ? lo : lr;
+                    const float m1 = sp == 0 ? mr : mo, l1 = sp == 0 ? lr : lo;
+                    float M = l0 > 0.f ? m0 : -CUDART_INF_F;
+                    if (l1 > 0.f) M = fmaxf(M, m1);
+                    float Lt = 0.f, w0 = 0.f, w1 = 0.f;
+                    if (M != -CUDART_INF_F) {
+                        if (l0 > 0.f) {
+                            w0 = exp2f(m0 - M);
+                            Lt = fmaf(w0, l0, Lt);
+                        }
+                        if (l1 > 0.f) {
+                            w1 = exp2f(m1 - M);
+                            Lt = fmaf(w1, l1, Lt);
+                        }
+                    }
+                    B.cwc[st][0] = w0;
+                    B.cwc[st][1] = w1;
+                    B.cwc[st][2] = Lt > 0.f ? 1.f / Lt : 0.f;
+                    if (rank == 0 && a.lse != nullptr)
+                        a.lse[qh0 + h] = Lt > 0.f ? (M + log2f(Lt)) * 0.6931471805599453f
+                                                  : -CUDART_INF_F;
+                }
+                pr::named_sync(kSoftBar, kSoftThreads);
+                // 64 heads x 256 d rows = 4096 16-byte chunks, 16 per thread,
+                // four at a time from each split.
+                const uint32_t os_l = hs::smem_u32(os);
+                const uint32_t os_r = pr::mapa(os_l, other);
+#pragma unroll 1
+                for (int i0 = 0; i0 < 16; i0 += 4) {
+                    float4 vl[4], vr[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = st + kSoftThreads * (i0 + k);
+                        const uint32_t off = uint32_t(((kHalfHeads * sp + (e >> 6)) * 256 + (e & 63) * 4) * 4);
+                        vl[k] = *reinterpret_cast<const float4*>(smem + kRingOff + off);
+                        vr[k] = pr::ld_remote_v4(os_r + off);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = st + kSoftThreads * (i0 + k);
+                        const int hl = e >> 6, dl = (e & 63) * 4;
+                        const float w0 = B.cwc[hl][0], w1 = B.cwc[hl][1], inv = B.cwc[hl][2];
+                        const float4 p0 = sp == 0 ? vl[k] : vr[k];
+                        const float4 p1 = sp == 0 ? vr[k] : vl[k];
+                        const float x = fmaf(w1, p1.x, w0 * p0.x) * inv;
+                        const float y = fmaf(w1, p1.y, w0 * p0.y) * inv;
+                        const float z = fmaf(w1, p1.z, w0 * p0.z) * inv;
+                        const float w = fmaf(w1, p1.w, w0 * p0.w) * inv;
+                        __nv_bfloat162 lo2 = __floats2bfloat162_rn(x, y);
+                        __nv_bfloat162 hi2 = __floats2bfloat162_rn(z, w);
+                        uint2 pk;
+                        pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+                        pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+                        const int d = 256 * (dl >> 7) + 128 * int(rank) + (dl & 127);
+                        *reinterpret_cast<uint2*>(a.out + (qh0 + kHalfHeads * sp + hl) * 512 + d) = pk;
+                    }
+                }
+            } else {
+                hs::set_status(a.status, HS_ERR_TIMEOUT);
+            }
+        } else if (!ok) {
             fail();
         } else {
             float* cw = reinterpret_cast<float*>(smem + kRingOff);  // [128][splits] + inv[128]
@@ -802,6 +920,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (st == 0) pr::bulk_wait();
         hs::tc::fence_before_sync();
     }
+    if constexpr (kClusterMerge) {
+        // The cluster merge's barrier, passed by the softmax warps in their
+        // epilogue and by the other warps here.
+        if (warp >= kSoftWarps) pr::cluster_sync();
+    }
     __syncthreads();
     pr::cluster_sync();  // no copy into the partner and no pair MMA is in flight past here
     if (warp == kCtlWarp) {
@@ -812,12 +935,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+int g_smem_set2[64] = {};
+int g_smem_set4[64] = {};
+int g_clusters4[64];
+bool g_clusters4_init = false;
+}  // namespace
+
+bool mla_pair_cluster_merge(int rows, int splits) {
+    if (splits != 2 || rows <= 0) return false;
+    // Only when every row's cluster of four is resident at once (the merge
+    // waits for the other pair of the cluster).
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!g_clusters4_init) {
+        for (int i = 0; i < 64; ++i) g_clusters4[i] = -1;
+        g_clusters4_init = true;
+    }
+    if (g_clusters4[dev] < 0) {
+        int n = 0;
+        if (hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(mla_pair_kernel<4>),
+                                         size_t(kSmemBytes), g_smem_set4) == HS_OK) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(4);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = size_t(kSmemBytes);
+            if (cudaOccupancyMaxActiveClusters(&n, mla_pair_kernel<4>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+        }
+        g_clusters4[dev] = n;
+    }
+    return rows <= g_clusters4[dev];
+}
+
 int launch_mla_pair(const MlaArgs& a, int pairs, hs_stream_t stream) {
-    static int smem_set[64] = {};
-    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(mla_pair_kernel),
-                                                size_t(kSmemBytes), smem_set);
+    if (mla_pair_cluster_merge(a.rows, a.splits)) {
+        const int rc = hs_host::ensure_dynamic_smem(
+            reinterpret_cast<const void*>(mla_pair_kernel<4>), size_t(kSmemBytes), g_smem_set4);
+        if (rc != HS_OK) return rc;
+        return hs_host::launch_pdl(mla_pair_kernel<4>, dim3(2 * pairs), dim3(kThreads),
+                                   size_t(kSmemBytes), stream, a);
+    }
+    const int rc = hs_host::ensure_dynamic_smem(reinterpret_cast<const void*>(mla_pair_kernel<2>),
+                                                size_t(kSmemBytes), g_smem_set2);
     if (rc != HS_OK) return rc;
-    return hs_host::launch_pdl(mla_pair_kernel, dim3(2 * pairs), dim3(kThreads),
+    return hs_host::launch_pdl(mla_pair_kernel<2>, dim3(2 * pairs), dim3(kThreads),
                                size_t(kSmemBytes), stream, a);
 }
 

@@ -143,6 +143,28 @@ __device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// Loads from another CTA's shared memory (after a cluster barrier).
+__device__ __forceinline__ float ld_remote_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_remote_s32(uint32_t cluster_addr) {
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_remote_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05, pair forms.
 __device__ __forceinline__ void tmem_alloc2(uint32_t* smem_dst, uint32_t ncols) {
@@ -172,13 +194,14 @@ __device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
-// One arrival on `bar` (same offset) in both CTAs once every pair MMA issued
-// so far by this thread has completed.
-__device__ __forceinline__ void commit2_both(uint64_t* bar) {
+// One arrival on `bar` (same offset) in both CTAs of the pair (cluster ranks
+// in `pair_mask`) once every pair MMA issued so far by this thread has
+// completed.
+__device__ __forceinline__ void commit2_both(uint64_t* bar, uint16_t pair_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
         "[%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(static_cast<unsigned short>(3))
+        "h"(pair_mask)
         : "memory");
 }
 

@@ -102,6 +102,28 @@ def test_mla_many_tiles_per_cta(rows, heads, cap):
                        sample_rows=[0, 1, rows // 2, rows - 1]) == 0
 
 
+@pytest.mark.parametrize("rows", [6, 37])
+def test_mla_128_heads_two_splits(rows):
+    """128 heads with lists of 257..512 rows: two splits per row.  Up to the
+    number of co-resident clusters of four CTAs (6 rows), a row's two CTA
+    pairs are one cluster and merge through distributed shared memory; 37
+    rows run as separate pairs merged through global memory.  Rows with an
+    empty list, with one tile only (the second split empty), a ragged tail
+    and the full 512 rows, every row checked."""
+    rng = np.random.default_rng(700 + rows)
+    n_kv, cap = 6000, 500
+    q = inputs.randn_bf16((rows, 128, 576), 70 + rows, device="cuda")
+    cache = inputs.randn_bf16((n_kv, 576), 71, device="cuda")
+    kv_rows = np.full((rows, 1, cap), -1, np.int32)
+    count = np.zeros((rows, 1), np.int32)
+    sizes = [0, 1, 128, 129, 300, cap] + [int(x) for x in rng.integers(200, cap + 1, rows)]
+    for r in range(rows):
+        n = sizes[r]
+        kv_rows[r, 0, :n] = rng.choice(n_kv, size=n, replace=False)
+        count[r, 0] = n
+    assert decode_both(q, cache, cache, kv_rows, count, 1 / 24, 512, 576, 0) == 0
+
+
 def test_single_candidate_and_tail_sizes():
     rng = np.random.default_rng(11)
     n_kv = 400

@@ -24,10 +24,11 @@ pytestmark = pytest.mark.gpu
 
 
 def test_capacity_limit_is_rejected_on_the_host():
-    # The workspace of this shape (two splits at least, on any GPU with two
-    # or more SMs) exceeds the built-in array; the call is refused before any
-    # device work, whatever the pointers.
-    rows, heads, cap = 32, 128, 65536
+    # The workspace of this shape (eight splits of each 128-head row, merged
+    # through partial states in the workspace, on a GPU with 64 or more SMs)
+    # exceeds the built-in array; the call is refused before any device
+    # work, whatever the pointers.
+    rows, heads, cap = 8, 128, 65536
     need = hs.sparse_decode_workspace_bytes(rows, heads, 1, cap, 576, 512)
     assert need > hs.NOALLOC_WORKSPACE_BYTES
     P = None
