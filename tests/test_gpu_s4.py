@@ -124,6 +124,24 @@ def test_mla_128_heads_two_splits(rows):
     assert decode_both(q, cache, cache, kv_rows, count, 1 / 24, 512, 576, 0) == 0
 
 
+def test_mla_16_heads_two_splits():
+    """16 heads, 64 rows of up to 300 candidates: two splits per row, merged
+    with eq. (7) by the split that finishes last.  Empty, 1-row, one-tile,
+    two-tile and ragged lists, every row checked."""
+    rng = np.random.default_rng(640)
+    rows, n_kv, cap = 64, 6000, 300
+    q = inputs.randn_bf16((rows, 16, 576), 72, device="cuda")
+    cache = inputs.randn_bf16((n_kv, 576), 73, device="cuda")
+    kv_rows = np.full((rows, 1, cap), -1, np.int32)
+    count = np.zeros((rows, 1), np.int32)
+    sizes = [0, 1, 128, 129, 256, 257, cap] + [int(x) for x in rng.integers(1, cap + 1, rows)]
+    for r in range(rows):
+        n = sizes[r]
+        kv_rows[r, 0, :n] = rng.choice(n_kv, size=n, replace=False)
+        count[r, 0] = n
+    assert decode_both(q, cache, cache, kv_rows, count, 1 / 24, 512, 576, 0) == 0
+
+
 def test_single_candidate_and_tail_sizes():
     rng = np.random.default_rng(11)
     n_kv = 400

@@ -119,8 +119,11 @@ def all_entry_points(q, cache, kv_rows, count, sample, label):
 # Shapes: (rows, heads, cap).  rows * heads / HG units against the SM count
 # decide the splits; every shape leaves at least two tiles per CTA.  With
 # 128 heads, 40 rows run one split per CTA pair and 30 rows two splits (the
-# pairs of a row merge inside one cluster).
-SHAPES = [(40, 16, 2048), (40, 32, 1536), (40, 128, 1024), (30, 128, 1024), (6, 20, 700)]
+# pairs of a row merge inside one cluster); with 16 heads, 64 rows run two
+# splits per row (the split that finishes last merges, in the finishing
+# pass together with two earlier partial columns).
+SHAPES = [(40, 16, 2048), (64, 16, 1024), (40, 32, 1536), (40, 128, 1024), (30, 128, 1024),
+          (6, 20, 700)]
 
 
 @pytest.mark.parametrize("rows,heads,cap", SHAPES)
