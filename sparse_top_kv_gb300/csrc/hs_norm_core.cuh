@@ -100,6 +100,10 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
     // the table's copy below; later chunks, if any, are loaded where they
     // are used.
     const int32_t req = a.row_req[row];
+    const bool has_req = req >= 0 && req < a.num_reqs;
+    // The request's length is loaded with the table below (both depend on
+    // the request only), not after the barrier.
+    const int32_t t_len = has_req ? a.seq_lens[req] : 0;
     int32_t tv0[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -107,7 +111,6 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
         tv0[u] = i < a.n_cand ? __ldg(cand + i) : -1;
     }
     if (tid < 4) s_err[tid] = 0;
-    const bool has_req = req >= 0 && req < a.num_reqs;
     const int32_t* table = has_req ? a.block_table + int64_t(req) * a.bt_stride : nullptr;
     if (has_req && a.stage_table) {
         // One coalesced copy of the row; every later lookup hits shared memory.
@@ -123,7 +126,7 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
         for (int i = tid; i < a.n_cand; i += NT) bad += (cand[i] != -1);
         if (bad) atomicAdd(&s_err[0], bad);
     } else {
-        const int64_t T = max(a.seq_lens[req], 0);
+        const int64_t T = max(t_len, 0);
         const int64_t a_hi = hs::min64(a.num_sinks, T);        // sinks  [0, a_hi)
         const int64_t s2 = hs::max64(hs::max64(T - a.window, 0), a_hi);  // window [s2, T)
 
