@@ -5,7 +5,8 @@
 // Math: PaperTrace 5.1.1 "从索引到 Kernel" section 3.1 eqs. (4)-(6) (tile
 // logits, running maximum and exponent sums, rescaled accumulator), section
 // 3.2 (mask before the exponent; empty set -> zero output, LSE = -inf) and
-// eq. (7) (split-KV merge, in the epilogue of the split that finishes last);
+// eq. (7) (split-KV merge, inside the cluster or in the epilogue of the split
+// that finishes last);
 // "PagedAttention 与 RadixAttention" section 1.4 (exp2 with scale * log2 e).
 // K = all 576 columns of a row, V = its first 512.
 //
@@ -36,7 +37,11 @@
 //    tile's softmax.  The odd CTA's control thread relays its units' arrival
 //    (and its P's) to the even CTA's issuing thread; commits are multicast to
 //    both CTAs.
-//  * Splits of a long list run as separate pairs; the last pair of a row to
+//  * A row split in two runs as one cluster of four CTAs, the two splits its
+//    two pairs: each CTA parks its unnormalised O in its own shared memory,
+//    and after one cluster barrier the CTAs merge with eq. (7) through
+//    distributed shared memory, each its half of the heads for its d rows.
+//    Other split counts run as separate pairs; the last pair of a row to
 //    finish merges the others' partial states with eq. (7).
 // Every wait is bounded (HS_ERR_TIMEOUT in the status word on expiry).
 #include <cuda_bf16.h>
