@@ -21,6 +21,13 @@
 //    the same rows were read one tile earlier).  Re-reading V instead of
 //    keeping the 144 KB tile resident keeps several units in flight per SM,
 //    so the gathers of the next tile overlap this tile's softmax and MMAs.
+//    The first tile's units that own a ring slot are filled by the loader
+//    and softmax warps together (the softmax warps wait for its logits in
+//    any case); the list's length and ids are prefetched into L2 before the
+//    launch-chain wait.
+//  * Splits of a list merge with eq. (7) in the epilogue of the split that
+//    finishes last (arrival counter, partial states read from L2, every
+//    column group's loads in flight at once).
 //  * One MMA thread issues tcgen05.mma: S^T[128 tokens x HG] = K Q^T (M = 128
 //    tokens, N = HG heads, K = 576) into one of two TMEM buffers, and
 //    O^T[512 x HG] += V^T P^T (four M = 128 slices of d, K = 128 tokens, V
