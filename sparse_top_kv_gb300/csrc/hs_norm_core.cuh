@@ -95,26 +95,35 @@ __device__ int normalize_row(const NormArgs& a, const int row, int32_t* s_table,
     static_assert(kWpt * NT == kWindowWords, "bitmap words per thread");
     const int tid = threadIdx.x;
     const int32_t* cand = a.cand + int64_t(row) * a.n_cand;
-    // The request first (the table row and the length depend on it), then
-    // the first kUnroll candidates of this thread, whose latency overlaps
-    // the table's copy below; later chunks, if any, are loaded where they
-    // are used.
+    // The request, then the first kUnroll candidates of this thread, whose
+    // latency overlaps the table's copy below; later chunks, if any, are
+    // loaded where they are used.
     const int32_t req = a.row_req[row];
-    const bool has_req = req >= 0 && req < a.num_reqs;
-    // The request's length is loaded with the table below (both depend on
-    // the request only), not after the barrier.
-    const int32_t t_len = has_req ? a.seq_lens[req] : 0;
     int32_t tv0[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         const int i = tid + u * NT;
         tv0[u] = i < a.n_cand ? __ldg(cand + i) : -1;
     }
+    // One index row per request is the common layout (row r serves request
+    // r): the length and the table row of request `row` are loaded before
+    // the request id arrives, and loaded again for a row of another request.
+    const bool guess = row < a.num_reqs;
+    const int32_t t_guess = guess ? a.seq_lens[row] : 0;
+    if (guess && a.stage_table) {
+        const int32_t* tg = a.block_table + int64_t(row) * a.bt_stride;
+        for (int b = tid; b < a.max_blocks; b += NT) s_table[b] = __ldg(tg + b);
+    }
     if (tid < 4) s_err[tid] = 0;
+    const bool has_req = req >= 0 && req < a.num_reqs;
+    const bool same = guess && req == row;
+    const int32_t t_len = has_req ? (same ? t_guess : a.seq_lens[req]) : 0;
     const int32_t* table = has_req ? a.block_table + int64_t(req) * a.bt_stride : nullptr;
     if (has_req && a.stage_table) {
-        // One coalesced copy of the row; every later lookup hits shared memory.
-        for (int b = tid; b < a.max_blocks; b += NT) s_table[b] = __ldg(table + b);
+        // One coalesced copy of the row; every later lookup hits shared
+        // memory (each thread rewrites only the entries it wrote above).
+        if (!same)
+            for (int b = tid; b < a.max_blocks; b += NT) s_table[b] = __ldg(table + b);
         table = s_table;
     }
     __syncthreads();  // s_err and the staged table
