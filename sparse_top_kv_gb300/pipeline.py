@@ -112,9 +112,9 @@ class HiSparseDecoder:
         pool (every 4 KB page by default) into the (still empty) hot buffer
         with hs_swap_in, in chunks of at most the hot buffer's rows.
 
-        Measured on the GB300 machines used here (VMs whose GPU reaches host
-        memory through the IOMMU): the first GPU reads of a page of a freshly
-        allocated pinned pool run far below the link rate; a decoder whose
+        On GB300 virtual machines whose GPU reaches host memory through the
+        IOMMU, the first GPU reads of a page of a freshly allocated pinned
+        pool run far below the link rate (measured); a decoder whose
         pool had only one row per 64 KB read beforehand ran its first steps
         3x slower than a later decoder over the same pool.  A server pays that
         once at start-up; this pass pays it at set-up so that a decode step
